@@ -1,0 +1,44 @@
+"""Writes tests/golden/tiny_seed0.txt from the CPU oracle.
+
+The fixture is a regression record of the oracle on the small oracle-check
+layer (hidden 256, 16 experts, top-2, inter 128, all tensors from seed 0),
+for M = 1 and M = 4.  It lets a run on another host (the GPU machine is an
+Arm host) confirm that the oracle it builds there computes what the pinned
+oracle computed here.  Only the oracle and the seeded input generator are
+called.
+
+    python tests/golden/make_golden.py
+"""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, ROOT)
+
+from oracle.oracle import Oracle  # noqa: E402
+from weight_streaming_expert_gb300 import workloads as wl  # noqa: E402
+
+OUT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tiny_seed0.txt")
+
+
+def main():
+    orc = Oracle()
+    lines = ["# oracle output on the small oracle-check layer, seed 0 (see make_golden.py)",
+             "# M  idx[M*k]  w[M*k] (fp32 hex)  out[M*H] (bf16 hex)"]
+    for M in (1, 4):
+        w_r, w_gu, w_d, x = wl.tiny_case(M=M, seed=0)
+        res = orc.moe_forward(wl.bf16_bits(x), wl.bf16_bits(w_r), wl.bf16_bits(w_gu),
+                              wl.bf16_bits(w_d), wl.TINY.topk)
+        lines.append(f"M {M}")
+        lines.append("idx " + " ".join(str(int(v)) for v in res["idx"].ravel()))
+        lines.append("w " + " ".join(f"{int(v):08x}" for v in res["w"].ravel().view(np.uint32)))
+        lines.append("out " + " ".join(f"{int(v):04x}" for v in res["out"].ravel()))
+    with open(OUT, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    print("wrote", OUT)
+
+
+if __name__ == "__main__":
+    main()
