@@ -1,0 +1,541 @@
+"""Benchmark: cold-L2 microseconds per MoE-layer call and achieved HBM GB/s.
+
+Workload (default): the Ling-shaped verify step -- hidden 2560, 512 routed
+experts, top-8 softmax + renormalisation, SwiGLU inter 512, M = 6 tokens, bf16,
+weights N(0, 0.02) drawn per layer from seed 1000 + layer, tokens N(0, 1)
+redrawn per call from seed 1_000_000 + call.  Distinct layer weight sets are
+cycled (and each call reads a different x) so every call's weights come from
+HBM, not L2: between two calls of the same layer the other layers stream
+several times the L2 size.  One step = one layer call (router + top-k +
+compaction + gate/up + SwiGLU + down + combine).
+
+Timing: K calls are captured (PDL chains intact) into CUDA graphs of G calls
+and replayed; CUDA events on the launching stream bracket exactly K calls,
+with a barrier and a device synchronize on both sides; max over ranks.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--M 6] [--zipf]
+    python bench.py --impl reference     # the CPU oracle on the same workload
+    python bench.py --sweep               # M x routing sweep (writes JSON lines)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "cold-L2 µs/MoE-layer call and achieved HBM GB/s (% of GB300 peak) at M=1/6/16"
+UNIT = "µs/call"
+L2_BYTES = 126 * 1024 * 1024      # replaced by the device's value when a GPU is present
+
+
+# --------------------------------------------------------------- helpers --
+
+def algorithmic_bytes(hidden, n_experts, topk, inter, M, n_active):
+    """Bytes the layer must move per call: each distinct activated expert's
+    gate/up and down weights once, the router weight once, x in, out out and
+    the routing indices out.  Weights of experts nobody chose are not counted
+    (that is the work the routing avoids)."""
+    expert = 3 * hidden * inter * 2
+    return (n_active * expert + n_experts * hidden * 2 + 2 * M * hidden * 2 + M * topk * 4)
+
+
+def gateup_bytes(hidden, inter, M, n_active, topk):
+    """Algorithmic bytes of the gate/up kernel: its weights once per distinct
+    expert, x in, the activated rows h out."""
+    return n_active * 2 * inter * hidden * 2 + M * hidden * 2 + M * topk * inter * 2
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+GATEUP_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
+                  for f in ("expert_gateup.cu", "common.cuh", "kernels.cuh")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gateup_traffic.json")
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0, period_ms=50):
+        self.index, self.period_ms = index, period_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- setup --
+
+def dist_setup(n_gpus):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, ws, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, v):
+    if pg is None:
+        return v
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Workload:
+    """Distinct layers on the device plus pools of token batches."""
+
+    def __init__(self, shape, n_layers, M, pool, zipf, device, layer_seed0=1000):
+        import torch
+        from weight_streaming_expert_gb300 import MoELayer
+        from weight_streaming_expert_gb300 import workloads as wl
+        self.shape, self.M, self.device = shape, M, device
+        self.layers = []
+        for l in range(n_layers):
+            w_r, w_gu, w_d = wl.layer_weights(shape, seed=layer_seed0 + l, device=device)
+            self.layers.append(MoELayer(w_r, w_gu, w_d, topk=shape.topk))
+            del w_r, w_gu, w_d
+            torch.cuda.empty_cache()
+        self.set_routing(zipf)
+        self.new_pool(M, pool)
+
+    def set_routing(self, zipf):
+        from weight_streaming_expert_gb300 import workloads as wl
+        bias = wl.zipf_router_bias(self.shape.n_experts) if zipf else None
+        for layer in self.layers:
+            layer.set_router_bias(bias)
+        self.zipf = zipf
+
+    def new_pool(self, M, pool):
+        import torch
+        from weight_streaming_expert_gb300 import workloads as wl
+        self.M = M
+        H, k = self.shape.hidden, self.shape.topk
+        self.xs = [wl.tokens(M, H, seed=1_000_000 + i, device=self.device) for i in range(pool)]
+        self.outs = [torch.empty((M, H), dtype=torch.bfloat16, device=self.device) for _ in range(pool)]
+        self.idxs = [torch.empty((M, k), dtype=torch.int32, device=self.device) for _ in range(pool)]
+
+    def call(self, c, stream=None):
+        i = c % len(self.xs)
+        self.layers[c % len(self.layers)](self.xs[i], out=self.outs[i], topk_idx=self.idxs[i], stream=stream)
+
+    def close(self):
+        for layer in self.layers:
+            layer.close()
+        self.layers = []
+
+
+def n_layers_for(M, shape, l2_bytes, requested):
+    if requested:
+        return requested
+    # distinct layers so that >= 3 x L2 of other layers' weights stream
+    # between two calls of the same layer (at least 4)
+    est_active = min(M * shape.topk, shape.n_experts) * 0.85 + 1
+    per_call = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, est_active)
+    return max(4, int(math.ceil(3 * l2_bytes / per_call)) + 1)
+
+
+# ----------------------------------------------------------------- timing --
+
+def time_graph(wkl, steps, warmup, pg, graph_len=64, sample_clocks=False, gpu_index=0):
+    """Returns (ms_per_step, per-call distinct-expert counts of one graph)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for c in range(warmup):
+            wkl.call(c, stream=s)
+    s.synchronize()
+    G = min(graph_len, steps)
+    graphs = []
+    # one graph per distinct remainder so that EXACTLY `steps` calls are timed
+    full, rem = divmod(steps, G)
+    lens = ([G] if full else []) + ([rem] if rem else [])
+    for n in lens:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for c in range(n):
+                    wkl.call(c, stream=s)
+        graphs.append(g)
+    # untimed replay of each graph (first-launch upload)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    active = []
+    for c in range(G):
+        i = c % len(wkl.xs)
+        active.append(int(torch.unique(wkl.idxs[i]).numel()))
+    sampler = ClockSampler(gpu_index) if sample_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(full):
+            graphs[0].replay()
+        if rem:
+            graphs[-1].replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    barrier(pg)
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(pg, ms), active, clocks
+
+
+def time_kernels(wkl, calls):
+    """Per-kernel durations (ms) from events between the three launches."""
+    import torch
+    s = torch.cuda.Stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(calls)]
+    with torch.cuda.stream(s):
+        for c in range(calls):
+            i = c % len(wkl.xs)
+            layer = wkl.layers[c % len(wkl.layers)]
+            layer.forward_timed(wkl.xs[i], wkl.outs[i], wkl.idxs[i], evs[c], stream=s)
+    torch.cuda.synchronize()
+    t = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(3)] for ev in evs])
+    active = []
+    for c in range(calls):
+        active.append(int(torch.unique(wkl.idxs[c % len(wkl.xs)]).numel()))
+    return t, active
+
+
+def time_e2e(wkl, steps):
+    """Through the public API with host buffers: per call, the H2D copy of that
+    call's tokens from pinned memory, the layer, and the D2H copies of its
+    output and routing indices; events bracket all of it."""
+    import torch
+    M, H, k = wkl.M, wkl.shape.hidden, wkl.shape.topk
+    P = len(wkl.xs)
+    hx = [x.cpu().pin_memory() for x in wkl.xs]
+    ho = [torch.empty((M, H), dtype=torch.bfloat16).pin_memory() for _ in range(P)]
+    hi = [torch.empty((M, k), dtype=torch.int32).pin_memory() for _ in range(P)]
+    dx = [torch.empty((M, H), dtype=torch.bfloat16, device=wkl.device) for _ in range(P)]
+    s = torch.cuda.Stream()
+
+    def one(c):
+        i = c % P
+        dx[i].copy_(hx[i], non_blocking=True)
+        wkl.layers[c % len(wkl.layers)](dx[i], out=wkl.outs[i], topk_idx=wkl.idxs[i], stream=s)
+        ho[i].copy_(wkl.outs[i], non_blocking=True)
+        hi[i].copy_(wkl.idxs[i], non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for c in range(min(8, steps)):
+            one(c)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for c in range(steps):
+            one(c)
+        e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / steps
+    return us, M * H * 2, M * H * 2 + M * k * 4
+
+
+def oracle_call_us(shape, M, zipf, budget_s, host=None, max_calls=None):
+    """Mean wall time of the CPU oracle on one layer call, timed on samples of
+    ONE token each (the oracle's work is linear in M, so a call costs M of
+    them).  Returns (us_per_call, n_samples, host_weights)."""
+    from oracle.oracle import Oracle
+    from weight_streaming_expert_gb300 import workloads as wl
+    orc = Oracle()
+    if host is None:
+        w_r, w_gu, w_d = wl.layer_weights(shape, seed=1000, device="cuda" if _has_cuda() else "cpu")
+        host = (wl.bf16_bits(w_r), wl.bf16_bits(w_gu), wl.bf16_bits(w_d))
+        del w_r, w_gu, w_d
+    bias = wl.zipf_router_bias(shape.n_experts).numpy() if zipf else None
+    xs = [wl.bf16_bits(wl.tokens(1, shape.hidden, seed=1_000_000 + i)) for i in range(64)]
+    orc.moe_forward(xs[0], *host, shape.topk, bias=bias)     # warm caches
+    times = []
+    t_start = time.perf_counter()
+    i = 0
+    while True:
+        t0 = time.perf_counter()
+        orc.moe_forward(xs[i % len(xs)], *host, shape.topk, bias=bias)
+        times.append(time.perf_counter() - t0)
+        i += 1
+        if max_calls is not None and i >= max_calls:
+            break
+        if time.perf_counter() - t_start > budget_s and i >= 3:
+            break
+    per_token = statistics.mean(times)
+    return per_token * M * 1e6, len(times), host
+
+
+def _has_cuda():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# ------------------------------------------------------------------ arms --
+
+def run_ours(args):
+    import torch
+    from weight_streaming_expert_gb300 import workloads as wl
+    rank, ws, local, pg = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    prop = torch.cuda.get_device_properties(dev)
+    l2 = getattr(prop, "L2_cache_size", L2_BYTES) or L2_BYTES
+    shape = wl.LING
+    M = args.M
+    n_layers = n_layers_for(M, shape, l2, args.layers)
+    wkl = Workload(shape, n_layers, M, args.pool, args.zipf, dev)
+    ms, active, clocks = time_graph(wkl, args.steps, args.warmup, pg, sample_clocks=(rank == 0),
+                                    gpu_index=local)
+    mean_active = float(np.mean(active))
+    bytes_call = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, mean_active)
+    us = ms * 1000.0
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+    # per-kernel durations (eager launches, events between kernels)
+    kt, kact = time_kernels(wkl, min(256, max(16, args.steps)))
+    kt_mean = kt.mean(axis=0) * 1000.0       # us: router, gate/up, down
+    gu_bytes = float(np.mean([gateup_bytes(shape.hidden, shape.inter, M, a, shape.topk) for a in kact]))
+    gu_gbs = gu_bytes / (kt_mean[1] * 1e-6) / 1e9
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("source_hash") == source_hash(GATEUP_SOURCES) and tr.get("M") == M:
+            traffic = tr.get("bytes_per_launch")
+    e2e_us, h2d, d2h = (None, 0, 0)
+    if not args.no_e2e:
+        e2e_us, h2d, d2h = time_e2e(wkl, min(args.steps, 4000))
+        e2e_us = max_over_ranks(pg, e2e_us)
+    by_m = {}
+    if args.all_m and rank == 0:
+        for m2, z2 in ((1, False), (16, True)):
+            wkl.set_routing(z2)
+            wkl.new_pool(m2, args.pool)
+            ms2, act2, _ = time_graph(wkl, min(args.steps, 4000), args.warmup, None)
+            b2 = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, m2, float(np.mean(act2)))
+            by_m[f"M={m2}" + ("_zipf" if z2 else "")] = {
+                "us_per_call": round(ms2 * 1000, 3), "achieved_gbs": round(b2 / (ms2 * 1e-3) / 1e9, 1),
+                "frac_of_peak": round(b2 / (ms2 * 1e-3) / 1e9 / peak, 4),
+                "mean_active_experts": round(float(np.mean(act2)), 2)}
+        wkl.set_routing(args.zipf)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        wkl.close()
+        torch.cuda.empty_cache()
+        us_cpu, n, _ = oracle_call_us(shape, M, args.zipf, args.cpu_budget)
+        cpu = {"value": round(us_cpu, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} single-token calls of the CPU oracle on layer seed 1000 "
+                         f"(x seeds 1e6+i), mean x M={M}; single-threaded C++"}
+    else:
+        wkl.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens (random init, no checkpoint)",
+            "config": {"workload": f"Ling-shaped MoE {'block-verify' if M >= 16 else 'verify' if M > 1 else 'decode'} step: "
+                                   f"hidden 2560, 512 experts, top-8 softmax+renorm, SwiGLU inter 512, "
+                                   f"M={M}, {'Zipf(1.1) router bias' if args.zipf else 'uniform routing'}",
+                       "M": M, "layers_cycled": n_layers, "x_pool": args.pool,
+                       "l2_policy": f"inputs larger than L2: {n_layers} distinct layer weight sets cycled, "
+                                    f"fresh x per call; L2 {l2 // (1024 * 1024)} MiB",
+                       "graph_calls": min(64, args.steps), "parallelism": f"replicas x{ws}"},
+            "achieved_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "peak_gbs": peak, "peak_kind": peak_kind,
+            "mean_active_experts": round(mean_active, 2), "algorithmic_bytes_per_call": int(bytes_call),
+            "kernel_us": {"router_topk_compact": round(kt_mean[0], 3), "gateup_swiglu": round(kt_mean[1], 3),
+                          "down_combine": round(kt_mean[2], 3), "timing": "eager, no PDL, events between launches"},
+            "roofline": {"bound": "hbm", "kernel": "gateup_swiglu", "achieved": round(gu_gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gu_gbs / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": int(gu_bytes), "peak_kind": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": None if e2e_us is None else {"value": round(e2e_us, 3), "unit": UNIT,
+                                                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+        }
+        if by_m:
+            line["by_M"] = by_m
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: same metric, unit and workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from weight_streaming_expert_gb300 import workloads as wl
+    shape = wl.LING
+    budget = args.cpu_budget
+    # warmup samples (untimed), then timed samples bounded by the budget
+    us_w, _, host = oracle_call_us(shape, args.M, args.zipf, budget_s=0.0,
+                                   max_calls=max(1, min(args.warmup, 3)))
+    us, n, _ = oracle_call_us(shape, args.M, args.zipf, budget_s=budget, host=host,
+                              max_calls=max(1, args.steps))
+    cores = 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 0,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate over bf16",
+        "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens",
+        "config": {"workload": f"Ling-shaped MoE step: hidden 2560, 512 experts, top-8, inter 512, M={args.M}",
+                   "M": args.M},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} single-token oracle calls (of {args.steps} requested steps, "
+                                   f"bounded to {budget:.0f} s), mean x M={args.M}"},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_sweep(args):
+    import torch
+    from weight_streaming_expert_gb300 import workloads as wl
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    shape = wl.LING
+    peak, peak_kind = measured_peaks()
+    wkl = Workload(shape, args.layers or 8, 1, args.pool, False, dev)
+    for zipf in (False, True):
+        wkl.set_routing(zipf)
+        for M in (1, 2, 4, 6, 8, 16, 32, 64):
+            wkl.new_pool(M, args.pool)
+            ms, active, _ = time_graph(wkl, args.steps, args.warmup, None)
+            kt, kact = time_kernels(wkl, 64)
+            b = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, float(np.mean(active)))
+            gb = b / (ms * 1e-3) / 1e9
+            gu = float(np.mean([gateup_bytes(shape.hidden, shape.inter, M, a, shape.topk) for a in kact]))
+            print(json.dumps({"sweep": True, "M": M, "routing": "zipf" if zipf else "uniform",
+                              "us_per_call": round(ms * 1000, 3), "achieved_gbs": round(gb, 1),
+                              "frac_of_peak": round(gb / peak, 4), "peak_kind": peak_kind,
+                              "mean_active_experts": round(float(np.mean(active)), 2),
+                              "kernel_us": [round(v, 3) for v in (kt.mean(axis=0) * 1000)],
+                              "gateup_gbs": round(gu / (kt.mean(axis=0)[1] * 1e-3) / 1e9, 1)}), flush=True)
+    wkl.close()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8192)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--M", type=int, default=6)
+    ap.add_argument("--zipf", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets (0 = auto)")
+    ap.add_argument("--pool", type=int, default=64, help="distinct token batches cycled")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-m", action="store_true", help="also time M=1 and M=16 (Zipf) in the same run")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle timing")
+    ap.add_argument("--sweep", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * moe.h -- C ABI of the GB300 small-M routed-MoE decode/verify layer.
+ *
+ * One call runs a whole routed-MoE layer for M = 1..64 tokens on one GPU:
+ *   router gate matvec -> softmax top-k with renormalisation -> on-device
+ *   token->expert compaction -> fused gate/up GEMV + SwiGLU -> down GEMV with
+ *   the routing-weighted combine in its epilogue.
+ * Three kernels, chained with Programmatic Dependent Launch, capturable in
+ * one CUDA graph.  No host synchronisation, no allocation and no
+ * device->host copy happens inside the forward call.
+ *
+ * Source of the method (page title and section):
+ *   "How Ling-3.0-flash reduces batch 1 decoding latency by 54% on 4
+ *   Blackwell GPUs" (mirror of the LMSYS post "Chasing the batch-1 floor:
+ *   Ling-3.0-flash speculative decode on Blackwell"):
+ *     - "Two kinds of idle": a batch-1 step is bounded by the cold read of
+ *       the activated expert weights plus the launch floor of small kernels;
+ *     - "PDL: the latency floor of stacked small kernels": the router chain
+ *       (gate matvec -> top-k) and the MoE chain (align -> up-GEMM ->
+ *       activation -> down-GEMM -> combine), producer-independent loads
+ *       issued before the dependency wait, the combine as an fp32 sum with
+ *       a single final cast;
+ *     - "Two fusions and a retune": the pair-axis token->expert bucketing
+ *       (stable in pair index, tail beyond the published total unwritten),
+ *       SwiGLU in the up-GEMM epilogue with a per-expert gate/up row
+ *       interleave applied at weight load;
+ *     - "bf16 router gate and lm_head": the router weight is bf16;
+ *     - "Economics of speculation at batch 1": verifying M tokens reads the
+ *       same weights as verifying one, so one weight pass serves all M.
+ *
+ * Conventions for every entry point:
+ *   - bf16 means IEEE bfloat16 (1-8-7), 2 bytes, little endian.
+ *   - "device" pointers are CUDA device (or managed) memory of the current
+ *     device; "host" pointers are ordinary host memory.
+ *   - Integer status returns are moe_status_t values; 0 is success.
+ *   - After any non-zero return, moe_last_error() gives a thread-local
+ *     description of the failure.
+ *   - A handle is not thread-safe: use one handle from one host thread and
+ *     one stream at a time.
+ *   - The target is sm_103a (GB300).  Other devices are refused at create.
+ */
+#ifndef WSE_MOE_H
+#define WSE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same representation as cudaStream_t / cudaEvent_t (opaque pointers), so
+ * callers need no CUDA header to use this ABI. */
+typedef struct CUstream_st* moe_stream_t;
+typedef struct CUevent_st* moe_event_t;
+
+typedef struct moe_layer moe_layer_t; /* opaque; owned by the library */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or handle     */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid request outside what this build runs */
+  MOE_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed       */
+  MOE_ERR_OOM = 4,            /* device allocation failed at create         */
+  MOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded in-kernel wait gave up           */
+} moe_status_t;
+
+/* Largest M accepted by one forward call (the workspace is sized for it). */
+#define MOE_MAX_TOKENS 64
+
+/* Flags for moe_forward_ex. */
+#define MOE_FWD_NO_PDL 0x1u /* launch the three kernels without PDL        */
+#define MOE_FWD_GRAPH 0x2u  /* replay a per-(handle, M) CUDA graph instead of
+                               three launches; the graph is captured on first
+                               use and updated when the pointers change       */
+
+/*
+ * moe_create -- build a layer handle from bf16 weights.
+ *
+ * Defines the layer of the "PDL: ..." section's router and MoE chains.
+ *   hidden     H: model width.  Must be a multiple of 256 with H/256 in
+ *              {1,2,4,5,8,10,12,16}; (2560 = Ling-3.0-flash width).
+ *   n_experts  E: routed experts, topk <= E <= 1024.
+ *   topk       k: experts per token, 1 <= k <= 32.
+ *   inter      I: expert intermediate width, one of {128, 256, 512}.
+ *   w_router   device bf16 [E][H], row e = router row of expert e
+ *              (the hidden -> n_experts mapping, stored one row per expert).
+ *   w_gate_up  device bf16 [E][2I][H]; rows [0,I) are the gate projection,
+ *              rows [I,2I) the up projection of each expert.
+ *   w_down     device bf16 [E][H][I]; the down projection of each expert.
+ * Ownership: the library COPIES the weights into its own device memory
+ *   (re-laid out for streaming: gate/up rows interleaved per expert as in
+ *   "Two fusions and a retune", fragment order for the tensor-core loads);
+ *   the caller may free its buffers when this returns.  The call is
+ *   synchronous on the current device and allocates that device's memory
+ *   (weights ~= the input size, plus a few MB of workspace).
+ * Returns NULL on error (moe_last_error() says why): invalid sizes or
+ *   pointers, a device other than sm_103, or allocation failure.
+ */
+moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter,
+                        const void* w_router, const void* w_gate_up,
+                        const void* w_down);
+
+/*
+ * moe_forward -- run the layer on M tokens, asynchronously on `stream`.
+ *   x         device bf16 [M][H], 16-byte aligned, read only.
+ *   out       device bf16 [M][H]: out[m] = bf16( sum_j w[m][j] * y_j ),
+ *             y_j = W_d[e_j] (silu(W_g[e_j] x[m]) * (W_u[e_j] x[m])),
+ *             fp32 accumulation, one final rounding ("PDL: ..." section,
+ *             single-cast combine).  Must not overlap x.
+ *   topk_idx  device int32 [M][k]: the chosen experts of each token in
+ *             descending router-logit order, ties to the lower expert id.
+ *   M         0 <= M <= MOE_MAX_TOKENS; M = 0 is a no-op returning MOE_OK.
+ *   stream    CUDA stream (NULL = legacy default stream).
+ * The routing weights are the softmax over all E logits renormalised over
+ * the chosen k.  No host sync, allocation or device->host copy: the call can
+ * be captured into a caller's CUDA graph.  Errors: MOE_ERR_INVALID_ARG for a
+ * NULL handle/pointer or misalignment, MOE_ERR_UNSUPPORTED for M > 64,
+ * MOE_ERR_CUDA if a launch fails.  Device-side wait timeouts are reported
+ * later by moe_get_status().
+ */
+int moe_forward(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx,
+                int M, moe_stream_t stream);
+
+/*
+ * moe_forward_ex -- moe_forward with options.
+ *   topk_w  NULL, or device fp32 [M][k] receiving the routing weights.
+ *   flags   MOE_FWD_NO_PDL and/or MOE_FWD_GRAPH.
+ * Results are bitwise identical for every flag combination (PDL and graph
+ * replay change scheduling only).  MOE_FWD_GRAPH on a stream that is being
+ * captured by the caller falls back to plain launches (they join the
+ * caller's graph).
+ */
+int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx,
+                   float* topk_w, int M, moe_stream_t stream, unsigned flags);
+
+/*
+ * moe_forward_timed -- profiling variant: plain launches without PDL, with
+ * ev[0] recorded before the router kernel, ev[1] after it, ev[2] after the
+ * gate/up kernel and ev[3] after the down/combine kernel, all on `stream`.
+ * ev must point to 4 valid events.  Same results as moe_forward.
+ */
+int moe_forward_timed(moe_layer_t* h, const void* x, void* out,
+                      int32_t* topk_idx, int M, moe_stream_t stream,
+                      moe_event_t* ev);
+
+/*
+ * moe_set_router_bias -- optional per-expert router bias.
+ *   bias  device fp32 [E] added to every logit before selection and softmax
+ *         (the "router top-k prefetches its bias" of the "PDL: ..."
+ *         section), or NULL to remove it.  The values are copied
+ *         (synchronously); the caller keeps ownership of `bias`.
+ */
+int moe_set_router_bias(moe_layer_t* h, const float* bias);
+
+/*
+ * moe_get_status -- synchronises the device, then returns and clears the
+ * handle's sticky device error word: MOE_OK, or MOE_ERR_DEVICE_TIMEOUT if a
+ * bounded wait inside a kernel gave up (the outputs of that call are then
+ * undefined).  Not for the hot path.
+ */
+int moe_get_status(moe_layer_t* h);
+
+/* Layer facts for tests and benchmarks (all host values). */
+typedef struct {
+  int hidden, n_experts, topk, inter;
+  int max_tokens;          /* MOE_MAX_TOKENS */
+  int n_sms;               /* SMs of the device the handle lives on */
+  int gateup_stages;       /* shared-memory ring depth of the gate/up kernel */
+  int down_stages;         /* ring depth of the down/combine kernel */
+  int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 rows x H) */
+  int down_tile_bytes;     /* bytes of one down weight tile (16 rows x I) */
+  size_t weight_bytes;     /* device bytes held for the weights */
+  size_t workspace_bytes;  /* device bytes held for the workspace */
+  int kernels_per_forward; /* kernel launches per forward call */
+} moe_info_t;
+
+int moe_get_info(const moe_layer_t* h, moe_info_t* out);
+
+/*
+ * moe_read_routing -- copy the last forward call's on-device compaction to
+ * host memory (synchronises the device; test aid, not the hot path).
+ * The compaction is the pair-axis bucketing of "Two fusions and a retune":
+ * the NP = M*k (token, slot) pairs sorted by expert id, stable in pair index
+ * p = token*k + slot, split into groups of at most 16 pairs per expert.
+ *   n_groups, n_active   host int*: groups written, distinct experts.
+ *   grp_expert, grp_start, grp_cnt   host int32 [cap]: per group its expert,
+ *                        first sorted position and pair count (<= 16).
+ *   pair_list            host int32 [M*k]: pair id at each sorted position.
+ *   pair_w               host fp32 [M*k]: routing weight of each pair id.
+ *   cap                  capacity of the grp_* arrays (>= M*k suffices).
+ */
+int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
+                     int32_t* grp_expert, int32_t* grp_start, int32_t* grp_cnt,
+                     int32_t* pair_list, float* pair_w, int cap);
+
+/* moe_destroy -- synchronises the handle's device, frees everything.
+ * NULL is a no-op. */
+void moe_destroy(moe_layer_t* h);
+
+/* Thread-local text of the last error set on this thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* WSE_MOE_H */

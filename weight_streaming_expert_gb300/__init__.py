@@ -1,1 +1,16 @@
-"""GB300-native small-M routed-MoE decode/verify layer (see include/moe.h)."""
+"""GB300-native small-M routed-MoE decode/verify layer.
+
+The layer (router GEMV -> softmax top-k -> SwiGLU experts -> weighted
+combine) runs in hand-written sm_103a CUDA kernels behind the C ABI in
+``include/moe.h``; ``MoELayer`` is its Python face.  Importing the package
+loads nothing; the CUDA library is loaded (and must exist) on first use.
+"""
+
+__all__ = ["MoELayer"]
+
+
+def __getattr__(name):
+    if name == "MoELayer":
+        from .layer import MoELayer
+        return MoELayer
+    raise AttributeError(name)

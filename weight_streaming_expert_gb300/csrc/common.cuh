@@ -1,0 +1,144 @@
+// common.cuh -- sm_103a building blocks shared by the layer's kernels:
+// mbarrier + bulk-copy (TMA) staging, Programmatic Dependent Launch control,
+// the bf16 tensor-core MMA, and the workspace shared by the three kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace wse {
+
+// ------------------------------------------------------------ limits ----
+constexpr int kMaxTokens = 64;        // M per forward call
+constexpr int kMaxTopk = 32;          // k
+constexpr int kMaxExperts = 1024;     // E
+constexpr int kMaxPairs = kMaxTokens * kMaxTopk;
+constexpr int kGroupTokens = 16;      // pairs per compaction group (one m16 / 2 x n8 tile)
+constexpr int kConsumerWarps = 8;
+constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
+constexpr int kRouterThreads = 256;   // 8 warps, one expert row each
+constexpr int kRouterExpertsPerCta = kRouterThreads / 32;
+constexpr int kGateUpTileRows = 8;    // 4 gate rows interleaved with 4 up rows
+constexpr int kDownTileRows = 16;
+constexpr int kMaxGateUpStages = 7;   // < kConsumerWarps: see the reduction-slot argument
+constexpr int kMaxDownStages = 16;
+constexpr uint32_t kBulkChunk = 16384;  // bytes per cp.async.bulk
+
+// A bounded wait gives up after this long (the kernels run for microseconds;
+// reaching it means a bug, never a slow call).
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+// Bits of the sticky device status word.
+enum : int {
+  kErrTimeoutFull = 1,    // consumer waited too long for a staged tile
+  kErrTimeoutEmpty = 2,   // producer waited too long for a free stage
+  kErrTimeoutReduce = 4,  // gate/up reducer waited too long for partials
+  kErrBadIndex = 8,       // a routing index read from the workspace was out of range
+};
+
+// Device workspace of one layer handle (all device pointers).
+struct Workspace {
+  int* status;        // [1] sticky error bits
+  int* router_count;  // [1] CTAs of the router kernel that finished (last-CTA-done)
+  int* n_groups;      // [1] compaction groups published for this call
+  int* n_active;      // [1] distinct experts this call
+  int* grp_expert;    // [kMaxPairs]
+  int* grp_start;     // [kMaxPairs] first sorted position of the group
+  int* grp_cnt;       // [kMaxPairs] pairs in the group (1..16)
+  int* pair_list;     // [kMaxPairs] pair id (token*k + slot) at each sorted position
+  float* pair_w;      // [kMaxPairs] routing weight by pair id
+  float* logits;      // [kMaxTokens][E]
+  __nv_bfloat16* h;   // [kMaxPairs][I] activated rows, sorted-position order
+  float* y;           // [kMaxPairs][H] weighted down-projection rows, by pair id
+  int* slab_count;    // [H/16] groups finished per 16-row output slab
+};
+
+// ------------------------------------------------------------- PTX -----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Programmatic Dependent Launch.  wait: block until every prerequisite grid
+// has completed and its memory is visible.  launch_dependents: allow the
+// next grid in the stream to be scheduled (its own wait still fences on our
+// completion).  Both are no-ops for a launch without the PDL attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity to complete; false after the
+// timeout (the caller records an error bit and leaves its loop).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+// Bulk (TMA) copy global -> shared, completion counted in bytes on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_chunked(uint32_t dst, const uint8_t* src, uint32_t bytes,
+                                                 uint32_t bar) {
+  for (uint32_t off = 0; off < bytes; off += kBulkChunk) {
+    uint32_t n = bytes - off < kBulkChunk ? bytes - off : kBulkChunk;
+    bulk_g2s(dst + off, src + off, n, bar);
+  }
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16x2 (low element first in memory) -> two fp32, exact.
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ void set_error(int* status, int bits) { atomicOr(status, bits); }
+
+}  // namespace wse

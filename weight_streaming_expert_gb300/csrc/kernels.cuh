@@ -1,0 +1,58 @@
+// kernels.cuh -- argument blocks and launch-side declarations of the layer's
+// three forward kernels and the create-time weight re-layout kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace wse {
+
+struct RouterArgs {
+  const __nv_bfloat16* x;         // [M][H]
+  const __nv_bfloat16* w_router;  // [E][H]
+  const float* bias;              // [E] or nullptr
+  int M, H, E, K;
+  int32_t* topk_idx;              // [M][K] caller output
+  float* topk_w;                  // [M][K] caller output or nullptr
+  Workspace ws;
+};
+
+struct GateUpArgs {
+  const uint8_t* w_gate_up;  // packed gate/up tiles, see pack.cu
+  const __nv_bfloat16* x;    // [M][H]
+  int M, H, I, K, E;
+  int stages;                // ring depth
+  uint32_t tile_bytes;       // 8 rows x H x 2
+  Workspace ws;
+};
+
+struct DownArgs {
+  const uint8_t* w_down;     // packed down tiles, see pack.cu
+  __nv_bfloat16* out;        // [M][H]
+  int M, H, I, K, E;
+  int stages;
+  uint32_t tile_bytes;       // 16 rows x I x 2
+  Workspace ws;
+};
+
+// Router: grid ceil(E/8) x 256 threads, dynamic smem router_smem_bytes().
+// CPL = H/256 (16-byte chunks of the expert row per lane).
+using RouterKernel = void (*)(RouterArgs);
+RouterKernel router_kernel_for(int cpl);
+size_t router_smem_bytes(int M, int E, int K);
+
+// Gate/up + SwiGLU: grid = #SMs x kExpertThreads.  KPW = H/256.
+using GateUpKernel = void (*)(GateUpArgs);
+GateUpKernel gateup_kernel_for(int kpw);
+size_t gateup_smem_bytes(int stages, uint32_t tile_bytes);
+
+// Down + combine: grid = #SMs x kExpertThreads.  KS = I/16.
+using DownKernel = void (*)(DownArgs);
+DownKernel down_kernel_for(int ks);
+size_t down_smem_bytes(int stages, uint32_t tile_bytes);
+
+// Create-time re-layout (pack.cu).
+void pack_gate_up(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int I, int H,
+                  cudaStream_t s);
+void pack_down(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int H, int I, cudaStream_t s);
+
+}  // namespace wse

@@ -1,0 +1,476 @@
+// moe_api.cu -- host runtime behind include/moe.h: argument checks, weight
+// re-layout at create, workspace, the three PDL-chained launches, and the
+// per-(handle, M) CUDA graph cache.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+
+#include "kernels.cuh"
+#include "moe.h"
+
+using namespace wse;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+void set_err(const char* fmt, ...) __attribute__((format(printf, 1, 2)));
+void set_err(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side fault injection for tests: MOE_FAULT_INJECT=alloc:N makes the
+// N-th device allocation of a moe_create call fail (N >= 1).
+struct AllocCounter {
+  int fail_at = 0, n = 0;
+  AllocCounter() {
+    const char* s = std::getenv("MOE_FAULT_INJECT");
+    if (s && std::strncmp(s, "alloc:", 6) == 0) fail_at = std::atoi(s + 6);
+  }
+  cudaError_t alloc(void** p, size_t bytes) {
+    ++n;
+    if (fail_at > 0 && n == fail_at) {
+      *p = nullptr;
+      return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+  }
+};
+
+struct GraphEntry {
+  cudaGraphExec_t exec = nullptr;
+  const void* x = nullptr;
+  void* out = nullptr;
+  int32_t* idx = nullptr;
+  float* tw = nullptr;
+  unsigned flags = 0;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct moe_layer {
+  int H = 0, E = 0, K = 0, I = 0;
+  int dev = 0, n_sms = 0;
+  __nv_bfloat16* w_router = nullptr;
+  uint8_t* w_gu = nullptr;  // packed gate/up tiles
+  uint8_t* w_d = nullptr;   // packed down tiles
+  float* bias = nullptr;
+  void* ws_mem = nullptr;
+  size_t ws_bytes = 0, weight_bytes = 0;
+  Workspace ws{};
+  int s2 = 0, s3 = 0;
+  uint32_t tile2 = 0, tile3 = 0;
+  size_t smem2 = 0, smem3 = 0;
+  RouterKernel k1 = nullptr;
+  GateUpKernel k2 = nullptr;
+  DownKernel k3 = nullptr;
+  std::map<int, GraphEntry> graphs;
+  cudaStream_t cap_stream = nullptr;
+};
+
+namespace {
+
+void drop_graphs(moe_layer* h);
+
+void free_layer(moe_layer* h) {
+  if (!h) return;
+  drop_graphs(h);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  cudaFree(h->w_router);
+  cudaFree(h->w_gu);
+  cudaFree(h->w_d);
+  cudaFree(h->bias);
+  cudaFree(h->ws_mem);
+  delete h;
+}
+
+void drop_graphs(moe_layer* h) {
+  for (auto& kv : h->graphs)
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+  h->graphs.clear();
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  set_err("%s: %s", what, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+// Enqueue the three kernels.  ev (4 events) brackets them for profiling.
+int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, int M,
+               cudaStream_t st, bool pdl, cudaEvent_t* ev) {
+  RouterArgs ra{};
+  ra.x = static_cast<const __nv_bfloat16*>(x);
+  ra.w_router = h->w_router;
+  ra.bias = h->bias;
+  ra.M = M; ra.H = h->H; ra.E = h->E; ra.K = h->K;
+  ra.topk_idx = idx;
+  ra.topk_w = tw;
+  ra.ws = h->ws;
+
+  GateUpArgs ga{};
+  ga.w_gate_up = h->w_gu;
+  ga.x = ra.x;
+  ga.M = M; ga.H = h->H; ga.I = h->I; ga.K = h->K; ga.E = h->E;
+  ga.stages = h->s2;
+  ga.tile_bytes = h->tile2;
+  ga.ws = h->ws;
+
+  DownArgs da{};
+  da.w_down = h->w_d;
+  da.out = static_cast<__nv_bfloat16*>(out);
+  da.M = M; da.H = h->H; da.I = h->I; da.K = h->K; da.E = h->E;
+  da.stages = h->s3;
+  da.tile_bytes = h->tile3;
+  da.ws = h->ws;
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c{};
+  c.stream = st;
+  c.attrs = pdl ? attr : nullptr;
+  c.numAttrs = pdl ? 1 : 0;
+
+  cudaError_t e;
+  if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event record");
+  c.gridDim = dim3((h->E + kRouterExpertsPerCta - 1) / kRouterExpertsPerCta);
+  c.blockDim = dim3(kRouterThreads);
+  c.dynamicSmemBytes = router_smem_bytes(M, h->E, h->K);
+  if ((e = cudaLaunchKernelEx(&c, h->k1, ra)) != cudaSuccess)
+    return cuda_fail(e, "router launch");
+  if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event record");
+  c.gridDim = dim3(h->n_sms);
+  c.blockDim = dim3(kExpertThreads);
+  c.dynamicSmemBytes = h->smem2;
+  if ((e = cudaLaunchKernelEx(&c, h->k2, ga)) != cudaSuccess) return cuda_fail(e, "gate/up launch");
+  if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event record");
+  c.dynamicSmemBytes = h->smem3;
+  if ((e = cudaLaunchKernelEx(&c, h->k3, da)) != cudaSuccess) return cuda_fail(e, "down launch");
+  if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return cuda_fail(e, "event record");
+  return MOE_OK;
+}
+
+int check_forward_args(moe_layer* h, const void* x, const void* out, const int32_t* idx, int M) {
+  if (!h) { set_err("null handle"); return MOE_ERR_INVALID_ARG; }
+  if (M < 0) { set_err("M = %d < 0", M); return MOE_ERR_INVALID_ARG; }
+  if (M > MOE_MAX_TOKENS) { set_err("M = %d exceeds %d", M, MOE_MAX_TOKENS); return MOE_ERR_UNSUPPORTED; }
+  if (M == 0) return MOE_OK;
+  if (!x || !out || !idx) { set_err("null x/out/topk_idx"); return MOE_ERR_INVALID_ARG; }
+  if (!aligned16(x)) { set_err("x must be 16-byte aligned"); return MOE_ERR_INVALID_ARG; }
+  if ((reinterpret_cast<uintptr_t>(out) & 1u) || (reinterpret_cast<uintptr_t>(idx) & 3u)) {
+    set_err("out must be 2-byte and topk_idx 4-byte aligned");
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const void* w_router,
+                        const void* w_gate_up, const void* w_down) {
+  g_last_error.clear();
+  // ---- argument checks (no CUDA call before these pass) ----
+  if (hidden <= 0 || hidden % 256 != 0 || !gateup_kernel_for(hidden / 256)) {
+    set_err("hidden = %d unsupported: need a multiple of 256 with hidden/256 in {1,2,4,5,8,10,12,16}",
+            hidden);
+    return nullptr;
+  }
+  if (inter <= 0 || inter % 16 != 0 || !down_kernel_for(inter / 16)) {
+    set_err("inter = %d unsupported: need one of {128, 256, 512}", inter);
+    return nullptr;
+  }
+  if (topk < 1 || topk > kMaxTopk) { set_err("topk = %d outside [1, %d]", topk, kMaxTopk); return nullptr; }
+  if (n_experts < topk || n_experts > kMaxExperts) {
+    set_err("n_experts = %d outside [topk, %d]", n_experts, kMaxExperts);
+    return nullptr;
+  }
+  if (!w_router || !w_gate_up || !w_down) { set_err("null weight pointer"); return nullptr; }
+
+  // ---- device ----
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { cuda_fail(e, "cudaGetDevice"); return nullptr; }
+  cudaDeviceProp prop;
+  if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) { cuda_fail(e, "device properties"); return nullptr; }
+  if (prop.major != 10 || prop.minor != 3) {
+    set_err("device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev, prop.major, prop.minor);
+    return nullptr;
+  }
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, router_kernel_for(hidden / 256))) != cudaSuccess) {
+    cuda_fail(e, "kernel image");
+    return nullptr;
+  }
+
+  moe_layer* h = new moe_layer;
+  h->H = hidden; h->E = n_experts; h->K = topk; h->I = inter;
+  h->dev = dev;
+  h->n_sms = prop.multiProcessorCount;
+  h->k1 = router_kernel_for(hidden / 256);
+  h->k2 = gateup_kernel_for(hidden / 256);
+  h->k3 = down_kernel_for(inter / 16);
+  h->tile2 = (uint32_t)(kGateUpTileRows * hidden * 2);
+  h->tile3 = (uint32_t)(kDownTileRows * inter * 2);
+
+  // Ring depths: the gate/up kernel takes what the opt-in shared memory
+  // allows (it never shares an SM with the down kernel); the down kernel
+  // leaves ~32 KB so the next layer's router CTAs can co-reside with it and
+  // prefetch their weights under its tail.
+  const size_t optin = prop.sharedMemPerBlockOptin;
+  h->s2 = (int)std::min<size_t>(kMaxGateUpStages, (optin - gateup_smem_bytes(0, h->tile2)) / h->tile2);
+  const size_t down_budget = std::min<size_t>(optin, prop.sharedMemPerMultiprocessor - 36 * 1024);
+  h->s3 = (int)std::min<size_t>(kMaxDownStages, (down_budget - down_smem_bytes(0, h->tile3)) / h->tile3);
+  if (h->s2 < 2 || h->s3 < 2) {
+    set_err("not enough shared memory for the staging rings");
+    free_layer(h);
+    return nullptr;
+  }
+  h->smem2 = gateup_smem_bytes(h->s2, h->tile2);
+  h->smem3 = down_smem_bytes(h->s3, h->tile3);
+
+  AllocCounter ac;
+  const size_t E = n_experts, H = hidden, I = inter;
+  const size_t b_router = E * H * 2, b_gu = E * 2 * I * H * 2, b_d = E * H * I * 2;
+  h->weight_bytes = b_router + b_gu + b_d;
+  if (ac.alloc((void**)&h->w_router, b_router) != cudaSuccess ||
+      ac.alloc((void**)&h->w_gu, b_gu) != cudaSuccess ||
+      ac.alloc((void**)&h->w_d, b_d) != cudaSuccess) {
+    cudaGetLastError();
+    set_err("device allocation of %zu weight bytes failed", h->weight_bytes);
+    free_layer(h);
+    return nullptr;
+  }
+
+  // workspace carve-up
+  const size_t np = (size_t)kMaxTokens * topk;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  const size_t o_status = take(4), o_count = take(4), o_ng = take(4), o_na = take(4);
+  const size_t o_ge = take(np * 4), o_gs = take(np * 4), o_gc = take(np * 4);
+  const size_t o_pl = take(np * 4), o_pw = take(np * 4);
+  const size_t o_lg = take((size_t)kMaxTokens * E * 4);
+  const size_t o_h = take(np * I * 2);
+  const size_t o_y = take(np * H * 4);
+  const size_t o_sc = take((H / kDownTileRows) * 4);
+  h->ws_bytes = off;
+  if (ac.alloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    set_err("device allocation of %zu workspace bytes failed", h->ws_bytes);
+    free_layer(h);
+    return nullptr;
+  }
+  uint8_t* base = static_cast<uint8_t*>(h->ws_mem);
+  h->ws.status = reinterpret_cast<int*>(base + o_status);
+  h->ws.router_count = reinterpret_cast<int*>(base + o_count);
+  h->ws.n_groups = reinterpret_cast<int*>(base + o_ng);
+  h->ws.n_active = reinterpret_cast<int*>(base + o_na);
+  h->ws.grp_expert = reinterpret_cast<int*>(base + o_ge);
+  h->ws.grp_start = reinterpret_cast<int*>(base + o_gs);
+  h->ws.grp_cnt = reinterpret_cast<int*>(base + o_gc);
+  h->ws.pair_list = reinterpret_cast<int*>(base + o_pl);
+  h->ws.pair_w = reinterpret_cast<float*>(base + o_pw);
+  h->ws.logits = reinterpret_cast<float*>(base + o_lg);
+  h->ws.h = reinterpret_cast<__nv_bfloat16*>(base + o_h);
+  h->ws.y = reinterpret_cast<float*>(base + o_y);
+  h->ws.slab_count = reinterpret_cast<int*>(base + o_sc);
+
+  cudaStream_t s = nullptr;
+  if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess) {
+    cuda_fail(e, "stream create");
+    free_layer(h);
+    return nullptr;
+  }
+  h->cap_stream = s;
+  bool ok = cudaMemsetAsync(h->ws_mem, 0, h->ws_bytes, s) == cudaSuccess &&
+            cudaMemcpyAsync(h->w_router, w_router, b_router, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  if (ok) {
+    pack_gate_up(static_cast<const __nv_bfloat16*>(w_gate_up), reinterpret_cast<__nv_bfloat16*>(h->w_gu),
+                 n_experts, inter, hidden, s);
+    pack_down(static_cast<const __nv_bfloat16*>(w_down), reinterpret_cast<__nv_bfloat16*>(h->w_d),
+              n_experts, hidden, inter, s);
+    ok = cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
+  }
+  if (!ok) {
+    set_err("weight re-layout failed: %s", cudaGetErrorString(cudaGetLastError()));
+    free_layer(h);
+    return nullptr;
+  }
+  if ((e = cudaFuncSetAttribute(h->k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem2)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(h->k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem3)) != cudaSuccess) {
+    cuda_fail(e, "shared-memory attribute");
+    free_layer(h);
+    return nullptr;
+  }
+  return h;
+}
+
+int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, float* topk_w, int M,
+                   moe_stream_t stream, unsigned flags) {
+  int rc = check_forward_args(h, x, out, topk_idx, M);
+  if (rc != MOE_OK || M == 0) return rc;
+  if (topk_w && (reinterpret_cast<uintptr_t>(topk_w) & 3u)) {
+    set_err("topk_w must be 4-byte aligned");
+    return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool pdl = !(flags & MOE_FWD_NO_PDL);
+  if (flags & MOE_FWD_GRAPH) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "capture status");
+    if (cs == cudaStreamCaptureStatusNone) {
+      GraphEntry& ge = h->graphs[M];
+      if (!ge.exec || ge.x != x || ge.out != out || ge.idx != topk_idx || ge.tw != topk_w ||
+          ge.flags != flags) {
+        cudaGraph_t g = nullptr;
+        if ((e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
+          return cuda_fail(e, "begin capture");
+        rc = launch_all(h, x, out, topk_idx, topk_w, M, h->cap_stream, pdl, nullptr);
+        e = cudaStreamEndCapture(h->cap_stream, &g);
+        if (rc != MOE_OK) { if (g) cudaGraphDestroy(g); return rc; }
+        if (e != cudaSuccess) return cuda_fail(e, "end capture");
+        if (ge.exec) {
+          cudaGraphExecUpdateResultInfo info;
+          if (cudaGraphExecUpdate(ge.exec, g, &info) != cudaSuccess) {
+            cudaGetLastError();
+            cudaGraphExecDestroy(ge.exec);
+            ge.exec = nullptr;
+          }
+        }
+        if (!ge.exec && (e = cudaGraphInstantiate(&ge.exec, g, 0)) != cudaSuccess) {
+          cudaGraphDestroy(g);
+          return cuda_fail(e, "graph instantiate");
+        }
+        cudaGraphDestroy(g);
+        ge.x = x; ge.out = out; ge.idx = topk_idx; ge.tw = topk_w; ge.flags = flags;
+      }
+      if ((e = cudaGraphLaunch(ge.exec, st)) != cudaSuccess) return cuda_fail(e, "graph launch");
+      return MOE_OK;
+    }
+  }
+  return launch_all(h, x, out, topk_idx, topk_w, M, st, pdl, nullptr);
+}
+
+int moe_forward(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, int M, moe_stream_t stream) {
+  return moe_forward_ex(h, x, out, topk_idx, nullptr, M, stream, 0u);
+}
+
+int moe_forward_timed(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, int M,
+                      moe_stream_t stream, moe_event_t* ev) {
+  int rc = check_forward_args(h, x, out, topk_idx, M);
+  if (rc != MOE_OK) return rc;
+  if (!ev || !ev[0] || !ev[1] || !ev[2] || !ev[3]) { set_err("need 4 events"); return MOE_ERR_INVALID_ARG; }
+  if (M == 0) return MOE_OK;
+  return launch_all(h, x, out, topk_idx, nullptr, M, reinterpret_cast<cudaStream_t>(stream), false,
+                    reinterpret_cast<cudaEvent_t*>(ev));
+}
+
+int moe_set_router_bias(moe_layer_t* h, const float* bias) {
+  if (!h) { set_err("null handle"); return MOE_ERR_INVALID_ARG; }
+  cudaError_t e;
+  if (!bias) {
+    if (h->bias) {
+      if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "synchronize");
+      cudaFree(h->bias);
+      h->bias = nullptr;
+    }
+    drop_graphs(h);  // captured graphs hold the old pointer
+    return MOE_OK;
+  }
+  if (!h->bias && (e = cudaMalloc((void**)&h->bias, (size_t)h->E * 4)) != cudaSuccess) {
+    h->bias = nullptr;
+    set_err("bias allocation failed");
+    return MOE_ERR_OOM;
+  }
+  if ((e = cudaMemcpy(h->bias, bias, (size_t)h->E * 4, cudaMemcpyDefault)) != cudaSuccess)
+    return cuda_fail(e, "bias copy");
+  drop_graphs(h);
+  return MOE_OK;
+}
+
+int moe_get_status(moe_layer_t* h) {
+  if (!h) { set_err("null handle"); return MOE_ERR_INVALID_ARG; }
+  cudaError_t e;
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "synchronize");
+  int st = 0;
+  if ((e = cudaMemcpy(&st, h->ws.status, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "status read");
+  if (st) {
+    cudaMemset(h->ws.status, 0, 4);
+    set_err("device status bits 0x%x (1 stage wait, 2 free-stage wait, 4 reduction wait, 8 bad index)", st);
+    return (st & 7) ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
+  if (!h || !o) { set_err("null argument"); return MOE_ERR_INVALID_ARG; }
+  o->hidden = h->H; o->n_experts = h->E; o->topk = h->K; o->inter = h->I;
+  o->max_tokens = MOE_MAX_TOKENS;
+  o->n_sms = h->n_sms;
+  o->gateup_stages = h->s2;
+  o->down_stages = h->s3;
+  o->gateup_tile_bytes = (int)h->tile2;
+  o->down_tile_bytes = (int)h->tile3;
+  o->weight_bytes = h->weight_bytes;
+  o->workspace_bytes = h->ws_bytes;
+  o->kernels_per_forward = 3;
+  return MOE_OK;
+}
+
+int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active, int32_t* grp_expert,
+                     int32_t* grp_start, int32_t* grp_cnt, int32_t* pair_list, float* pair_w, int cap) {
+  if (!h || !n_groups || !n_active || M < 0 || M > MOE_MAX_TOKENS) {
+    set_err("bad argument");
+    return MOE_ERR_INVALID_ARG;
+  }
+  cudaError_t e;
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "synchronize");
+  if ((e = cudaMemcpy(n_groups, h->ws.n_groups, 4, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(n_active, h->ws.n_active, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "routing read");
+  const int ng = *n_groups < cap ? *n_groups : cap;
+  const size_t np = (size_t)M * h->K;
+  if (ng > 0 && grp_expert && (e = cudaMemcpy(grp_expert, h->ws.grp_expert, ng * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "routing read");
+  if (ng > 0 && grp_start && (e = cudaMemcpy(grp_start, h->ws.grp_start, ng * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "routing read");
+  if (ng > 0 && grp_cnt && (e = cudaMemcpy(grp_cnt, h->ws.grp_cnt, ng * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "routing read");
+  if (np > 0 && pair_list && (e = cudaMemcpy(pair_list, h->ws.pair_list, np * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "routing read");
+  if (np > 0 && pair_w && (e = cudaMemcpy(pair_w, h->ws.pair_w, np * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "routing read");
+  return MOE_OK;
+}
+
+void moe_destroy(moe_layer_t* h) {
+  if (!h) return;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  cudaSetDevice(h->dev);
+  cudaDeviceSynchronize();
+  free_layer(h);
+  cudaSetDevice(cur);
+}
+
+}  // extern "C"

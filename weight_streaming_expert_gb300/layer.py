@@ -1,0 +1,122 @@
+"""Python face of the C ABI: ``MoELayer`` wraps one ``moe_layer_t`` handle.
+
+PyTorch is used for device memory and streams only; tensors are passed to
+the library as raw device pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import native as N
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class MoELayer:
+    """One routed-MoE layer (router + top-k + SwiGLU experts + combine).
+
+    Weights (bf16, on the current CUDA device) are copied into the library at
+    construction; the caller's tensors may be freed afterwards.
+      w_router  [E, H]     w_gate_up [E, 2I, H] (gate rows first)   w_down [E, H, I]
+    """
+
+    def __init__(self, w_router, w_gate_up, w_down, topk: int):
+        E, H = w_router.shape
+        I = w_down.shape[2]
+        for t in (w_router, w_gate_up, w_down):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("weights must be contiguous bf16 CUDA tensors")
+        if tuple(w_gate_up.shape) != (E, 2 * I, H) or tuple(w_down.shape) != (E, H, I):
+            raise ValueError("weight shapes must be [E,H], [E,2I,H], [E,H,I]")
+        self.hidden, self.n_experts, self.topk, self.inter = H, E, topk, I
+        self.device = w_router.device
+        L = N.lib()
+        with torch.cuda.device(self.device):
+            h = L.moe_create(H, E, topk, I, _ptr(w_router), _ptr(w_gate_up), _ptr(w_down))
+        if not h:
+            raise N.MoEError("moe_create", N.MOE_ERR_INVALID_ARG, N.last_error())
+        self._h = ctypes.c_void_p(h)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self) -> N.moe_info_t:
+        o = N.moe_info_t()
+        N.check("moe_get_info", N.lib().moe_get_info(self._h, ctypes.byref(o)))
+        return o
+
+    def set_router_bias(self, bias):
+        """bias: fp32 [E] tensor (any device) or None."""
+        if bias is not None:
+            bias = bias.to(device=self.device, dtype=torch.float32).contiguous()
+        N.check("moe_set_router_bias", N.lib().moe_set_router_bias(self._h, _ptr(bias)))
+        torch.cuda.synchronize(self.device)
+
+    def forward(self, x, out=None, topk_idx=None, topk_w=None, stream=None, pdl=True, graph=False):
+        """x: bf16 [M, H] CUDA.  Returns (out [M,H] bf16, topk_idx [M,k] int32)."""
+        M = x.shape[0]
+        if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.shape[1] != self.hidden:
+            raise ValueError("x must be contiguous bf16 [M, hidden]")
+        if out is None:
+            out = torch.empty_like(x)
+        if topk_idx is None:
+            topk_idx = torch.empty((M, self.topk), dtype=torch.int32, device=x.device)
+        flags = (0 if pdl else N.MOE_FWD_NO_PDL) | (N.MOE_FWD_GRAPH if graph else 0)
+        rc = N.lib().moe_forward_ex(self._h, _ptr(x), _ptr(out), _ptr(topk_idx), _ptr(topk_w), M,
+                                    _stream_ptr(stream), flags)
+        N.check("moe_forward_ex", rc)
+        return out, topk_idx
+
+    __call__ = forward
+
+    def forward_timed(self, x, out, topk_idx, events, stream=None):
+        """Profiling launch: events = 4 torch.cuda.Event(enable_timing=True)."""
+        arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        rc = N.lib().moe_forward_timed(self._h, _ptr(x), _ptr(out), _ptr(topk_idx), x.shape[0],
+                                       _stream_ptr(stream), arr)
+        N.check("moe_forward_timed", rc)
+
+    def status(self) -> int:
+        """Synchronises; returns the sticky device status (0 = ok) and clears it."""
+        return N.lib().moe_get_status(self._h)
+
+    def read_routing(self, M: int):
+        """Last call's on-device compaction as numpy arrays (synchronises)."""
+        import numpy as np
+        cap = max(1, M * self.topk)
+        ng, na = ctypes.c_int(), ctypes.c_int()
+        ge = np.zeros(cap, np.int32)
+        gs = np.zeros(cap, np.int32)
+        gc = np.zeros(cap, np.int32)
+        pl = np.zeros(cap, np.int32)
+        pw = np.zeros(cap, np.float32)
+        i32 = ctypes.POINTER(ctypes.c_int32)
+        rc = N.lib().moe_read_routing(self._h, M, ctypes.byref(ng), ctypes.byref(na),
+                                      ge.ctypes.data_as(i32), gs.ctypes.data_as(i32), gc.ctypes.data_as(i32),
+                                      pl.ctypes.data_as(i32),
+                                      pw.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), cap)
+        N.check("moe_read_routing", rc)
+        n = ng.value
+        return dict(n_groups=n, n_active=na.value, grp_expert=ge[:n], grp_start=gs[:n], grp_cnt=gc[:n],
+                    pair_list=pl[:M * self.topk], pair_w=pw[:M * self.topk])
+
+    def close(self):
+        if getattr(self, "_h", None):
+            N.lib().moe_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
