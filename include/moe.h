@@ -138,7 +138,9 @@ int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx,
  * moe_forward_timed -- profiling variant: plain launches without PDL, with
  * ev[0] recorded before the router kernel, ev[1] after it, ev[2] after the
  * gate/up kernel and ev[3] after the down/combine kernel, all on `stream`.
- * ev must point to 4 valid events.  Same results as moe_forward.
+ * ev must point to 4 valid events.  Same results as moe_forward.  Under
+ * stream capture the records become event nodes of the graph, so a replay
+ * times the kernels with no host gap between them.
  */
 int moe_forward_timed(moe_layer_t* h, const void* x, void* out,
                       int32_t* topk_idx, int M, moe_stream_t stream,
@@ -169,7 +171,7 @@ typedef struct {
   int gateup_stages;       /* shared-memory ring depth of the gate/up kernel */
   int down_stages;         /* ring depth of the down/combine kernel */
   int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 rows x H) */
-  int down_tile_bytes;     /* bytes of one down weight tile (16 rows x I) */
+  int down_tile_bytes;     /* bytes of one down weight tile (8 rows x I) */
   size_t weight_bytes;     /* device bytes held for the weights */
   size_t workspace_bytes;  /* device bytes held for the workspace */
   int kernels_per_forward; /* kernel launches per forward call */

@@ -47,7 +47,10 @@ def run_and_check(orc, layer, host, x, k, bias=None, **kw):
     layer.set_router_bias(bias)
     out, idx = layer(x)
     torch.cuda.synchronize()
-    assert layer.status() == 0, "device status word set"
+    st = layer.status()
+    if st != 0:
+        from weight_streaming_expert_gb300 import native
+        raise AssertionError(f"device status {st}: {native.last_error()}")
     st = parity.check_layer(orc, bits(x), host["wr"], host["wgu"], host["wd"], k,
                             out.float().cpu().numpy(), idx.cpu().numpy(),
                             bias=None if bias is None else bias.cpu().numpy(), **kw)
@@ -278,12 +281,16 @@ def test_swiglu_epilogue_full_range(oracle, MoELayer):
     mism = 0
     subnormal_flush = 0
     total = 0
+    bad = []
     for c0 in range(0, all_g.shape[0], per_call):
         gv = all_g[c0:c0 + per_call]
         n = gv.shape[0]
         gate = np.zeros((E, I, H), np.uint16)
         up = np.zeros((E, I, H), np.uint16)
-        uvals = wl.bf16_bits(torch.from_numpy(rng.standard_normal(n).astype(np.float32)).to(torch.bfloat16))
+        # |u| < 1 keeps every silu(g) * u finite: an infinite h anywhere in a
+        # token's row would turn the identity down projection's 0 * h into NaN
+        uvals = wl.bf16_bits(torch.from_numpy(rng.uniform(-0.999, 0.999, n).astype(np.float32))
+                             .to(torch.bfloat16))
         # token m uses expert m % E and hidden position m; r = slot within I
         for i in range(n):
             m, r = divmod(i, I)
@@ -309,17 +316,25 @@ def test_swiglu_epilogue_full_range(oracle, MoELayer):
             u = float(parity.bf16_bits_to_f32(np.array([uvals[i]]))[0])
             want = oracle.swiglu_bf16(g, u)
             total += 1
-            if got[i] != want:
-                is_sub = (gv[i] & 0x7F80) == 0 and (gv[i] & 0x7F) != 0
-                if is_sub and got[i] in (0x0000, 0x8000):
-                    subnormal_flush += 1          # tensor-core input flush of a bf16 subnormal
-                elif abs(int(got[i]) - int(want)) <= 1:
-                    mism += 1                     # one bf16 step (fast exp vs libm exp)
-                else:
-                    raise AssertionError(f"g={g!r} u={u!r}: gpu {got[i]:#06x} oracle {want:#06x}")
+            # the sign of a zero h is not observable through the down
+            # projection (1 * -0 + 0 * h' = +0), so zeros compare unsigned
+            if got[i] == want or (got[i] & 0x7FFF) == 0 == (want & 0x7FFF):
+                continue
+            is_sub = (gv[i] & 0x7F80) == 0 and (gv[i] & 0x7F) != 0
+            if is_sub and (got[i] & 0x7FFF) == 0:
+                subnormal_flush += 1          # a bf16-subnormal gate value read as zero
+            elif abs(int(got[i]) - int(want)) <= 1:
+                mism += 1                     # one bf16 step (fast exp vs libm exp)
+            elif len(bad) < 20:
+                bad.append(f"g={g!r} u={u!r}: gpu {got[i]:#06x} oracle {want:#06x}")
+            else:
+                bad.append("...")
         layer.close()
     assert total == all_g.shape[0]
+    assert not bad, f"{len(bad)} epilogue results differ: " + "; ".join(bad[:20])
     assert mism <= 0.001 * total, f"{mism} of {total} differ by one bf16 step"
+    # every bf16 subnormal gate value (254 of them) may be read as zero
+    assert subnormal_flush <= 254
 
 
 def test_bad_arguments_on_device(ling):

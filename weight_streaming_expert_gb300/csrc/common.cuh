@@ -19,9 +19,9 @@ constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps +
 constexpr int kRouterThreads = 256;   // 8 warps, one expert row each
 constexpr int kRouterExpertsPerCta = kRouterThreads / 32;
 constexpr int kGateUpTileRows = 8;    // 4 gate rows interleaved with 4 up rows
-constexpr int kDownTileRows = 16;
+constexpr int kDownTileRows = 8;     // 8 output rows (n8) x I per down tile
 constexpr int kMaxGateUpStages = 7;   // < kConsumerWarps: see the reduction-slot argument
-constexpr int kMaxDownStages = 16;
+constexpr int kMaxDownStages = 24;    // a multiple of kConsumerWarps: each stage has one owner warp
 constexpr uint32_t kBulkChunk = 16384;  // bytes per cp.async.bulk
 
 // A bounded wait gives up after this long (the kernels run for microseconds;
@@ -39,8 +39,9 @@ enum : int {
 // Device workspace of one layer handle (all device pointers).
 struct Workspace {
   int* status;        // [1] sticky error bits
+  unsigned long long* diag;  // [4] first timeout: where, elapsed ns, raw barrier word, spare
   int* router_count;  // [1] CTAs of the router kernel that finished (last-CTA-done)
-  int* n_groups;      // [1] compaction groups published for this call
+  int* n_groups;      // [1] compaction groups published for this call (router's last CTA)
   int* n_active;      // [1] distinct experts this call
   int* grp_expert;    // [kMaxPairs]
   int* grp_start;     // [kMaxPairs] first sorted position of the group
@@ -50,7 +51,7 @@ struct Workspace {
   float* logits;      // [kMaxTokens][E]
   __nv_bfloat16* h;   // [kMaxPairs][I] activated rows, sorted-position order
   float* y;           // [kMaxPairs][H] weighted down-projection rows, by pair id
-  int* slab_count;    // [H/16] groups finished per 16-row output slab
+  int* slab_count;    // [H/8] groups finished per 8-row output slab
 };
 
 // ------------------------------------------------------------- PTX -----
@@ -95,17 +96,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete; false after the
 // timeout (the caller records an error bit and leaves its loop).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long* waited = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    const unsigned long long dt = global_timer_ns() - t0;
+    if (dt > kWaitTimeoutNs) {
+      if (waited) *waited = dt;
+      return false;
+    }
   }
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before its
+// later async-proxy (bulk copy) accesses -- needed before refilling a stage
+// that was just read with ordinary loads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Bulk (TMA) copy global -> shared, completion counted in bytes on `bar`.
@@ -140,5 +163,27 @@ __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v <
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __device__ __forceinline__ void set_error(int* status, int bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ unsigned long long mbar_raw(uint32_t bar) {
+  unsigned long long v;
+  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(bar) : "memory");
+  return v;
+}
+
+// Record the first bounded-wait timeout of a call (kernel id 1..3, wait kind
+// = the status bit, CTA, loop index, ring depth) and its evidence.
+__device__ __forceinline__ void record_timeout(const Workspace& ws, int kernel, int kind, int j,
+                                               int stages, uint32_t bar, unsigned long long waited) {
+  const unsigned long long where = ((unsigned long long)kernel << 56) |
+                                   ((unsigned long long)kind << 48) |
+                                   ((unsigned long long)blockIdx.x << 32) |
+                                   ((unsigned long long)(stages & 0xffff) << 16) | (unsigned)(j & 0xffff);
+  if (atomicCAS(ws.diag, 0ull, where) == 0ull) {
+    ws.diag[1] = waited;
+    ws.diag[2] = mbar_raw(bar);
+    ws.diag[3] = ((unsigned long long)threadIdx.x << 32) | (unsigned)gridDim.x;
+  }
+  set_error(ws.status, kind);
+}
 
 }  // namespace wse

@@ -15,11 +15,12 @@
 //    tile (bitwise neutral: every output column is an independent dot).
 //
 // GB300 design.
-//  * Work: the routed (expert, <=16-token group) list published by the
-//    router kernel, times 2I/8 tiles of 8 weight rows (4 gate rows
-//    interleaved with their 4 up rows) x the full hidden dim (40 KB at
-//    H = 2560).  The flat tile range is split evenly over a persistent grid
-//    of one CTA per SM; the count is read on the device, never on the host.
+//  * Work: the (expert, <=16-token group) list the router published, loaded
+//    into shared memory by every CTA (compaction.cuh), times
+//    2I/8 tiles of 8 weight rows (4 gate rows interleaved with their 4 up
+//    rows) x the full hidden dim (40 KB at H = 2560).  The flat tile range
+//    is split evenly over a persistent grid of one CTA per SM; the count is
+//    known only on the device, never on the host.
 //  * Streaming: one producer thread moves each tile HBM -> shared memory with
 //    bulk (TMA) copies into a ring of stages guarded by mbarriers, so up to
 //    (stages x 40 KB) per SM are in flight independent of the math warps.
@@ -36,28 +37,20 @@
 //    are (gate r, up r) thanks to the interleave, so no data moves.
 //  * Every wait is bounded; a timeout sets a sticky error bit and the CTA
 //    leaves its loop.
+#include "compaction.cuh"
 #include "kernels.cuh"
 
 namespace wse {
 
 namespace {
 
-struct StageMeta {
-  int start;  // first sorted position of the tile's group
-  int cnt;    // pairs in the group (1..16)
-  int tt;     // tile index inside the expert
-  int pad;
-  int tok[kGroupTokens];
-};
-
 constexpr int kRedSlots = 8;  // == kConsumerWarps; must exceed the ring depth
-constexpr size_t kMetaOff = 256;
-constexpr size_t kRedOff = 1024;
+constexpr size_t kRedOff = 256;
 constexpr size_t kRedBytes = (size_t)kRedSlots * kConsumerWarps * 32 * sizeof(float4);
 constexpr size_t kRingOff = kRedOff + kRedBytes;
-static_assert((2 * kMaxGateUpStages + kRedSlots) * 8 <= kMetaOff, "barrier area");
-static_assert(kMetaOff + kMaxGateUpStages * sizeof(StageMeta) <= kRedOff, "meta area");
+static_assert((2 * kMaxGateUpStages + kRedSlots) * 8 <= kRedOff, "barrier area");
 static_assert(kMaxGateUpStages < kRedSlots, "reduction slots must outnumber ring stages");
+static_assert(kRingOff % 128 == 0, "ring alignment");
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
@@ -67,9 +60,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxGateUpStages;
   uint64_t* redbar = empty + kMaxGateUpStages;
-  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + kMetaOff);
   float4* red = reinterpret_cast<float4*>(smem + kRedOff);
   uint8_t* ring = smem + kRingOff;
+  int* comp = reinterpret_cast<int*>(ring + (size_t)a.stages * a.tile_bytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
@@ -82,7 +75,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
     for (int r = 0; r < kRedSlots; ++r) mbar_init(smem_u32(&redbar[r]), kConsumerWarps);
     fence_mbar_init();
   }
-  __syncthreads();
 
   // The weights streamed here are chosen by the routing: nothing of the main
   // loop is producer-independent.  Wait for the router, then release the
@@ -90,14 +82,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
   pdl_wait();
   pdl_launch_dependents();
 
-  const int TPG = (2 * a.I) / kGateUpTileRows;  // tiles per group
   const int NP = a.M * a.K;
-  int n_groups = *a.ws.n_groups;
-  if (n_groups < 0 || n_groups > NP) {
-    if (threadIdx.x == 0) set_error(a.ws.status, kErrBadIndex);
-    n_groups = 0;
-  }
-  const long long T = (long long)n_groups * TPG;
+  const SmemRouting rt = load_routing(a.ws, NP, a.E, comp);
+
+  const int TPG = (2 * a.I) / kGateUpTileRows;  // tiles per group
+  const long long T = (long long)rt.n_groups * TPG;
   const int t0 = (int)(T * blockIdx.x / gridDim.x);
   const int t1 = (int)(T * (blockIdx.x + 1) / gridDim.x);
   const int n = t1 - t0;
@@ -106,46 +95,20 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
     // ---------------------------------------------------------- producer
     if (lane != 0) return;
     const uint32_t ring_u32 = smem_u32(ring);
-    int cg = -1, e = 0, start = 0, cnt = 1;
-    int tok[kGroupTokens];
     for (int j = 0; j < n; ++j) {
       const int s = j % S;
-      if (j >= S && !mbar_wait(smem_u32(&empty[s]), ((j / S) - 1) & 1)) {
-        set_error(a.ws.status, kErrTimeoutEmpty);
+      unsigned long long waited = 0;
+      if (j >= S && !mbar_wait(smem_u32(&empty[s]), ((j / S) - 1) & 1, &waited)) {
+        record_timeout(a.ws, 2, kErrTimeoutEmpty, j, S, smem_u32(&empty[s]), waited);
         break;
       }
       const int tile = t0 + j;
       const int g = tile / TPG, tt = tile - g * TPG;
-      if (g != cg) {
-        e = a.ws.grp_expert[g];
-        start = a.ws.grp_start[g];
-        cnt = a.ws.grp_cnt[g];
-        if (e < 0 || e >= a.E || cnt < 1 || cnt > kGroupTokens || start < 0 || start + cnt > NP) {
-          set_error(a.ws.status, kErrBadIndex);
-          e = 0; start = 0; cnt = 1;
-        }
-#pragma unroll
-        for (int i = 0; i < kGroupTokens; ++i) {
-          int p = i < cnt ? a.ws.pair_list[start + i] : 0;
-          if (p < 0 || p >= NP) { set_error(a.ws.status, kErrBadIndex); p = 0; }
-          tok[i] = p / a.K;
-        }
-        cg = g;
-      }
+      const int e = rt.grp_expert[g];
       const uint32_t fb = smem_u32(&full[s]);
-      // expect the bytes, start the copy, then publish the metadata and
-      // arrive: the phase completes only when both have happened.
-      asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(a.tile_bytes)
-                   : "memory");
+      mbar_arrive_expect_tx(fb, a.tile_bytes);
       bulk_g2s_chunked(ring_u32 + (uint32_t)s * a.tile_bytes,
                        a.w_gate_up + ((size_t)e * TPG + tt) * a.tile_bytes, a.tile_bytes, fb);
-      StageMeta& md = meta[s];
-      md.start = start;
-      md.cnt = cnt;
-      md.tt = tt;
-#pragma unroll
-      for (int i = 0; i < kGroupTokens; ++i) md.tok[i] = tok[i];
-      mbar_arrive(fb);
     }
     return;
   }
@@ -155,19 +118,18 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
   const uint32_t* xw = reinterpret_cast<const uint32_t*>(a.x);
   const int hw = a.H >> 1;  // 32-bit words per token row
   uint32_t af[KPW][2][4];
-  int cur_start = -1;
+  int cur_g = -1, start = 0, cnt = 0;
   for (int j = 0; j < n; ++j) {
     const int s = j % S;
-    if (!mbar_wait(smem_u32(&full[s]), (j / S) & 1)) {
-      set_error(a.ws.status, kErrTimeoutFull);
-      break;
-    }
-    const int start = meta[s].start, cnt = meta[s].cnt, tt = meta[s].tt;
-    if (start != cur_start) {
+    const int tile = t0 + j;
+    const int g = tile / TPG, tt = tile - g * TPG;
+    if (g != cur_g) {
       // A fragments (tokens x this warp's K slice) of the new group; rows
-      // beyond the group's count repeat token 0 and are never stored.
-      const int tok0 = meta[s].tok[g4 < cnt ? g4 : 0];
-      const int tok1 = meta[s].tok[g4 + 8 < cnt ? g4 + 8 : 0];
+      // beyond the group's count repeat its first token and are never stored.
+      start = rt.grp_start[g];
+      cnt = rt.grp_cnt[g];
+      const int tok0 = rt.pair_list[start + (g4 < cnt ? g4 : 0)] / a.K;
+      const int tok1 = rt.pair_list[start + (g4 + 8 < cnt ? g4 + 8 : 0)] / a.K;
       const uint32_t* x0 = xw + (size_t)tok0 * hw + t4;
       const uint32_t* x1 = xw + (size_t)tok1 * hw + t4;
 #pragma unroll
@@ -181,7 +143,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
           af[q][kk][3] = x1[kw + 4];
         }
       }
-      cur_start = start;
+      cur_g = g;
+    }
+    unsigned long long waited = 0;
+    if (!mbar_wait(smem_u32(&full[s]), (j / S) & 1, &waited)) {
+      record_timeout(a.ws, 2, kErrTimeoutFull, j, S, smem_u32(&full[s]), waited);
+      break;
     }
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
     const uint4* wp =
@@ -202,8 +169,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
     if (lane == 0) mbar_arrive(smem_u32(&redbar[slot]));
 
     if (warp == slot) {  // reducer of this tile (rotates over the warps)
-      if (!mbar_wait(smem_u32(&redbar[slot]), (j >> 3) & 1)) {
-        set_error(a.ws.status, kErrTimeoutReduce);
+      if (!mbar_wait(smem_u32(&redbar[slot]), (j >> 3) & 1, &waited)) {
+        record_timeout(a.ws, 2, kErrTimeoutReduce, j, S, smem_u32(&redbar[slot]), waited);
         break;
       }
       float4 acc = red[(slot * kConsumerWarps) * 32 + lane];
@@ -215,8 +182,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
         acc.z += v.z;
         acc.w += v.w;
       }
-      // (acc.x, acc.y) = (gate, up) of token g4, intermediate row 4*tt + t4;
-      // (acc.z, acc.w) the same for token g4 + 8.
+      // (acc.x, acc.y) = (gate, up) of group token g4, intermediate row
+      // 4*tt + t4; (acc.z, acc.w) the same for group token g4 + 8.
       const int r = 4 * tt + t4;
       if (g4 < cnt)
         a.ws.h[(size_t)(start + g4) * a.I + r] = __float2bfloat16_rn(silu(acc.x) * acc.y);
@@ -228,8 +195,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) gateup_swiglu_kernel(GateUp
 
 }  // namespace
 
-size_t gateup_smem_bytes(int stages, uint32_t tile_bytes) {
-  return kRingOff + (size_t)stages * tile_bytes;
+size_t gateup_smem_bytes(int stages, uint32_t tile_bytes, int NP, int E) {
+  (void)E;
+  return kRingOff + (size_t)stages * tile_bytes + routing_smem_ints(NP) * 4;
 }
 
 GateUpKernel gateup_kernel_for(int kpw) {

@@ -75,7 +75,7 @@ struct moe_layer {
   Workspace ws{};
   int s2 = 0, s3 = 0;
   uint32_t tile2 = 0, tile3 = 0;
-  size_t smem2 = 0, smem3 = 0;
+  size_t smem1 = 0, smem2 = 0, smem3 = 0;  // largest dynamic shared memory per kernel
   RouterKernel k1 = nullptr;
   GateUpKernel k2 = nullptr;
   DownKernel k3 = nullptr;
@@ -110,7 +110,8 @@ int cuda_fail(cudaError_t e, const char* what) {
   return MOE_ERR_CUDA;
 }
 
-// Enqueue the three kernels.  ev (4 events) brackets them for profiling.
+// Enqueue the three kernels.  ev (4 events) brackets them for profiling; the
+// records are external event nodes when the stream is being captured.
 int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, int M,
                cudaStream_t st, bool pdl, cudaEvent_t* ev) {
   RouterArgs ra{};
@@ -125,6 +126,7 @@ int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, 
   GateUpArgs ga{};
   ga.w_gate_up = h->w_gu;
   ga.x = ra.x;
+  ga.topk_idx = idx;
   ga.M = M; ga.H = h->H; ga.I = h->I; ga.K = h->K; ga.E = h->E;
   ga.stages = h->s2;
   ga.tile_bytes = h->tile2;
@@ -133,6 +135,7 @@ int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, 
   DownArgs da{};
   da.w_down = h->w_d;
   da.out = static_cast<__nv_bfloat16*>(out);
+  da.topk_idx = idx;
   da.M = M; da.H = h->H; da.I = h->I; da.K = h->K; da.E = h->E;
   da.stages = h->s3;
   da.tile_bytes = h->tile3;
@@ -147,21 +150,29 @@ int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, 
   c.numAttrs = pdl ? 1 : 0;
 
   cudaError_t e;
-  if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event record");
+  // under stream capture the records must be external event nodes
+  unsigned ev_flags = cudaEventRecordDefault;
+  if (ev) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(st, &cs)) != cudaSuccess) return cuda_fail(e, "capture status");
+    if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+  }
+  if (ev && (e = cudaEventRecordWithFlags(ev[0], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
   c.gridDim = dim3((h->E + kRouterExpertsPerCta - 1) / kRouterExpertsPerCta);
   c.blockDim = dim3(kRouterThreads);
-  c.dynamicSmemBytes = router_smem_bytes(M, h->E, h->K);
+  c.dynamicSmemBytes = router_smem_bytes(M, h->H, h->K, h->E);
   if ((e = cudaLaunchKernelEx(&c, h->k1, ra)) != cudaSuccess)
     return cuda_fail(e, "router launch");
-  if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event record");
+  if (ev && (e = cudaEventRecordWithFlags(ev[1], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
   c.gridDim = dim3(h->n_sms);
   c.blockDim = dim3(kExpertThreads);
-  c.dynamicSmemBytes = h->smem2;
+  c.dynamicSmemBytes = gateup_smem_bytes(h->s2, h->tile2, M * h->K, h->E);
   if ((e = cudaLaunchKernelEx(&c, h->k2, ga)) != cudaSuccess) return cuda_fail(e, "gate/up launch");
-  if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event record");
-  c.dynamicSmemBytes = h->smem3;
+  if (ev && (e = cudaEventRecordWithFlags(ev[2], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
+  c.blockDim = dim3(kDownThreadsPerCta);
+  c.dynamicSmemBytes = down_smem_bytes(h->s3, h->tile3, M * h->K, h->E, h->H);
   if ((e = cudaLaunchKernelEx(&c, h->k3, da)) != cudaSuccess) return cuda_fail(e, "down launch");
-  if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return cuda_fail(e, "event record");
+  if (ev && (e = cudaEventRecordWithFlags(ev[3], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
   return MOE_OK;
 }
 
@@ -231,21 +242,26 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   h->tile2 = (uint32_t)(kGateUpTileRows * hidden * 2);
   h->tile3 = (uint32_t)(kDownTileRows * inter * 2);
 
-  // Ring depths: the gate/up kernel takes what the opt-in shared memory
-  // allows (it never shares an SM with the down kernel); the down kernel
-  // leaves ~32 KB so the next layer's router CTAs can co-reside with it and
-  // prefetch their weights under its tail.
+  // Ring depths, sized for the largest call (M = MOE_MAX_TOKENS): both expert
+  // kernels take what the opt-in shared memory allows (one CTA per SM; deep
+  // rings keep enough bytes in flight to cover the loaded HBM latency).
   const size_t optin = prop.sharedMemPerBlockOptin;
-  h->s2 = (int)std::min<size_t>(kMaxGateUpStages, (optin - gateup_smem_bytes(0, h->tile2)) / h->tile2);
-  const size_t down_budget = std::min<size_t>(optin, prop.sharedMemPerMultiprocessor - 36 * 1024);
-  h->s3 = (int)std::min<size_t>(kMaxDownStages, (down_budget - down_smem_bytes(0, h->tile3)) / h->tile3);
-  if (h->s2 < 2 || h->s3 < 2) {
+  const int np_max = kMaxTokens * topk;
+  const size_t gu_fixed = gateup_smem_bytes(0, h->tile2, np_max, n_experts);
+  const size_t dn_fixed = down_smem_bytes(0, h->tile3, np_max, n_experts, hidden);
+  h->s2 = optin > gu_fixed ? (int)std::min<size_t>(kMaxGateUpStages, (optin - gu_fixed) / h->tile2) : 0;
+  const size_t down_budget = optin;
+  // down-kernel stages come in whole sets of one per consumer warp
+  h->s3 = down_budget > dn_fixed ? (int)std::min<size_t>(kMaxDownStages, (down_budget - dn_fixed) / h->tile3) : 0;
+  h->s3 -= h->s3 % kConsumerWarps;
+  if (h->s2 < 2 || h->s3 < kConsumerWarps) {
     set_err("not enough shared memory for the staging rings");
     free_layer(h);
     return nullptr;
   }
-  h->smem2 = gateup_smem_bytes(h->s2, h->tile2);
-  h->smem3 = down_smem_bytes(h->s3, h->tile3);
+  h->smem1 = router_smem_bytes(kMaxTokens, hidden, topk, n_experts);
+  h->smem2 = gateup_smem_bytes(h->s2, h->tile2, np_max, n_experts);
+  h->smem3 = down_smem_bytes(h->s3, h->tile3, np_max, n_experts, hidden);
 
   AllocCounter ac;
   const size_t E = n_experts, H = hidden, I = inter;
@@ -264,7 +280,7 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   const size_t np = (size_t)kMaxTokens * topk;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-  const size_t o_status = take(4), o_count = take(4), o_ng = take(4), o_na = take(4);
+  const size_t o_status = take(4), o_diag = take(32), o_count = take(4), o_ng = take(4), o_na = take(4);
   const size_t o_ge = take(np * 4), o_gs = take(np * 4), o_gc = take(np * 4);
   const size_t o_pl = take(np * 4), o_pw = take(np * 4);
   const size_t o_lg = take((size_t)kMaxTokens * E * 4);
@@ -280,6 +296,7 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   }
   uint8_t* base = static_cast<uint8_t*>(h->ws_mem);
   h->ws.status = reinterpret_cast<int*>(base + o_status);
+  h->ws.diag = reinterpret_cast<unsigned long long*>(base + o_diag);
   h->ws.router_count = reinterpret_cast<int*>(base + o_count);
   h->ws.n_groups = reinterpret_cast<int*>(base + o_ng);
   h->ws.n_active = reinterpret_cast<int*>(base + o_na);
@@ -314,8 +331,14 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
     free_layer(h);
     return nullptr;
   }
-  if ((e = cudaFuncSetAttribute(h->k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem2)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(h->k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem3)) != cudaSuccess) {
+  // The expert kernels run one CTA per SM with most of its shared memory;
+  // asking for the largest carveout up front avoids a reconfiguration of the
+  // L1/shared split between launches.
+  if ((e = cudaFuncSetAttribute(h->k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem1)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(h->k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem2)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(h->k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem3)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(h->k2, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(h->k3, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess) {
     cuda_fail(e, "shared-memory attribute");
     free_layer(h);
     return nullptr;
@@ -412,11 +435,18 @@ int moe_get_status(moe_layer_t* h) {
   cudaError_t e;
   if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "synchronize");
   int st = 0;
-  if ((e = cudaMemcpy(&st, h->ws.status, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+  unsigned long long dg[4] = {0, 0, 0, 0};
+  if ((e = cudaMemcpy(&st, h->ws.status, 4, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(dg, h->ws.diag, sizeof dg, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "status read");
   if (st) {
     cudaMemset(h->ws.status, 0, 4);
-    set_err("device status bits 0x%x (1 stage wait, 2 free-stage wait, 4 reduction wait, 8 bad index)", st);
+    cudaMemset(h->ws.diag, 0, sizeof dg);
+    set_err("device status bits 0x%x (1 stage wait, 2 free-stage wait, 4 reduction wait, 8 bad index); "
+            "first timeout: kernel %llu kind %llu cta %llu stages %llu index %llu waited %llu ns "
+            "barrier 0x%016llx thread %llu grid %llu",
+            st, dg[0] >> 56, (dg[0] >> 48) & 0xff, (dg[0] >> 32) & 0xffff, (dg[0] >> 16) & 0xffff,
+            dg[0] & 0xffff, dg[1], dg[2], dg[3] >> 32, dg[3] & 0xffffffffull);
     return (st & 7) ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_CUDA;
   }
   return MOE_OK;

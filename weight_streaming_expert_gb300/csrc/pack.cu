@@ -14,11 +14,11 @@
 //     elements    = row[32q+2t], [32q+2t+1], [32q+2t+8], [32q+2t+9],
 //                   row[32q+16+2t], [+1], [+8], [+9]
 //   i.e. the B fragments (k16 x n8, n = tile row) of k-steps 2q and 2q+1.
-// Down, per expert e and slab sl (rows 16sl .. 16sl+15), k-step kk:
-//   chunk (e, sl, kk, lane), rows R0 = 16sl + g, R1 = R0 + 8, kb = 16kk:
-//     R0[kb+2t], R0[kb+2t+1], R1[kb+2t], R1[kb+2t+1],
-//     R0[kb+2t+8], R0[kb+2t+9], R1[kb+2t+8], R1[kb+2t+9]
-//   i.e. the A fragment (m16 x k16, m = output row) of one k-step.
+// Down, per expert e and slab sl (output rows 8sl .. 8sl+7):
+//   16-byte chunk (e, sl, q, lane), row = 8sl + g:
+//     row[32q+2t], [+1], [+8], [+9], row[32q+16+2t], [+1], [+8], [+9]
+//   i.e. the B fragments (k16 x n8, n = output row) of k-steps 2q, 2q+1,
+//   the same packing as the gate/up tiles.
 #include "kernels.cuh"
 
 namespace wse {
@@ -59,26 +59,21 @@ __global__ void pack_gate_up_kernel(const uint16_t* __restrict__ src, uint4* __r
 
 __global__ void pack_down_kernel(const uint16_t* __restrict__ src, uint4* __restrict__ dst, int E,
                                  int H, int I) {
-  const int KS = I / 16, SL = H / 16;
-  const long long total = (long long)E * SL * KS * 32;
+  const int KP = I / 32, SL = H / 8;
+  const long long total = (long long)E * SL * KP * 32;
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < total;
        c += (long long)gridDim.x * blockDim.x) {
     const int lane = (int)(c & 31);
     long long r = c >> 5;
-    const int kk = (int)(r % KS);
-    r /= KS;
+    const int q = (int)(r % KP);
+    r /= KP;
     const int sl = (int)(r % SL);
     const long long e = r / SL;
     const int g = lane >> 2, t = lane & 3;
-    const uint16_t* s0 = src + ((size_t)e * H + 16 * sl + g) * I;
-    const uint16_t* s1 = s0 + (size_t)8 * I;
-    const int kb = 16 * kk + 2 * t;
-    uint4 v;
-    v.x = (uint32_t)s0[kb] | ((uint32_t)s0[kb + 1] << 16);          // a0: row g,   k 2t..2t+1
-    v.y = (uint32_t)s1[kb] | ((uint32_t)s1[kb + 1] << 16);          // a1: row g+8, k 2t..2t+1
-    v.z = (uint32_t)s0[kb + 8] | ((uint32_t)s0[kb + 9] << 16);      // a2: row g,   k 2t+8..
-    v.w = (uint32_t)s1[kb + 8] | ((uint32_t)s1[kb + 9] << 16);      // a3: row g+8, k 2t+8..
-    dst[c] = v;
+    const uint16_t* s = src + ((size_t)e * H + 8 * sl + g) * I;  // output row 8*sl + g
+    const int k0 = 32 * q + 2 * t, k1 = k0 + 16;
+    // (b0, b1) of k-step 2q, then (b0, b1) of k-step 2q+1
+    dst[c] = pack8(s, k0, k0 + 1, k0 + 8, k0 + 9, s, k1, k1 + 1, k1 + 8, k1 + 9);
   }
 }
 

@@ -1,5 +1,4 @@
-// router.cu -- router gate matvec + softmax top-k + on-device token->expert
-// compaction, in one launch.
+// router.cu -- router gate matvec + softmax top-k with renormalisation.
 //
 // Method (page "How Ling-3.0-flash reduces batch 1 decoding latency by 54%
 // on 4 Blackwell GPUs"):
@@ -9,25 +8,30 @@
 //    weight load does not depend on the producer, so it is issued BEFORE the
 //    dependency wait and the cold read flies under the producer's tail; the
 //    top-k prefetches its bias the same way.
-//  * "Two fusions and a retune" (moe_align on the pair axis): the M*k
-//    (token, slot) pairs are bucketed by expert with a rank that is stable in
-//    pair index, the bucket populations give bucket-ordered offsets and the
-//    published total; nothing is read back to the host and the tail beyond
-//    the published total is left unwritten.
 //
-// GB300 design: each warp owns one expert row (H bf16 in registers, 16-byte
-// coalesced loads), so E/8 CTAs of 8 warps read the 2.6 MB once.  The last
-// CTA to finish (a device-scope counter, no spin) does the top-k (one warp
-// per token: k rounds of a two-step redux.sync arg-max over register keys)
-// and the compaction (shared-memory histogram, one warp-wide scan, and a
-// stable in-bucket rank from __match_any_sync over 32-pair chunks).
+// GB300 design: each warp owns one expert row (H bf16 held in registers,
+// 16-byte coalesced loads), so E/8 CTAs of 8 warps read the 2.6 MB once.
+// The tokens are staged into shared memory in blocks of 8 with cp.async
+// (double-buffered, one round trip per block), and every warp takes its
+// dot products from there.  The last CTA to finish (a device-scope arrival
+// counter; no spin) runs the top-k: one warp per token, the E logits held
+// in registers, k rounds of a two-step redux.sync arg-max (largest value,
+// then lowest expert id) with a branch-free rescan of the winning lane.
+// The same CTA then builds the token->expert compaction block-wide in
+// shared memory and publishes it (compaction.cuh); every CTA of the expert
+// kernels loads it with one coalesced read.
+#include "compaction.cuh"
 #include "kernels.cuh"
 
 namespace wse {
 
-size_t router_smem_bytes(int M, int E, int K) {
-  const size_t np = (size_t)M * K;
-  return np * 8 + (size_t)E * 12;  // s_idx, s_w [NP]; s_cnt, s_off, s_run [E]
+constexpr int kRouterTokBlock = 8;  // tokens staged per shared-memory block
+
+size_t router_smem_bytes(int M, int H, int K, int E) {
+  const int rows = M <= kRouterTokBlock ? M : 2 * kRouterTokBlock;
+  const size_t stage = (size_t)rows * H * 2;
+  const size_t comp = compaction_smem_ints(M * K, E) * 4;  // last CTA, after the tokens
+  return stage > comp ? stage : comp;
 }
 
 namespace {
@@ -55,62 +59,53 @@ __device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float acc) {
   return acc;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// T tokens starting at m against the register-resident expert row.
-template <int CPL, int T>
-__device__ __forceinline__ void logits_tokens(const RouterArgs& a, const uint4 (&w)[CPL], int m,
-                                              int e, float bias, int lane) {
-  const uint4* xr[T];
-#pragma unroll
-  for (int t = 0; t < T; ++t)
-    xr[t] = reinterpret_cast<const uint4*>(a.x + (size_t)(m + t) * a.H) + lane;
-  float s[T];
-#pragma unroll
-  for (int t = 0; t < T; ++t) s[t] = 0.f;
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) s[t] = dot8(w[c], xr[t][c * 32], s[t]);
-  }
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    const float v = warp_sum(s[t]);
-    if (lane == 0) a.ws.logits[(size_t)(m + t) * a.E + e] = v + bias;
-  }
+// Stage tokens [8b, 8b+8) of x into shared buffer (b & 1).
+__device__ __forceinline__ void stage_tokens(const RouterArgs& a, uint4* xs, int b) {
+  const int hc = a.H >> 3;  // 16-byte chunks per token
+  const int m0 = b * kRouterTokBlock;
+  const int tb = min(kRouterTokBlock, a.M - m0);
+  uint4* dst = xs + (size_t)(b & 1) * kRouterTokBlock * hc;
+  const uint4* src = reinterpret_cast<const uint4*>(a.x) + (size_t)m0 * hc;
+  for (int i = threadIdx.x; i < tb * hc; i += blockDim.x) cp_async16(dst + i, src + i);
+  cp_async_commit();
 }
 
-// Top-k of token m by one warp.  Lane l holds the keys of experts l, l+32, ...
-// Round j selects the largest remaining value with two warp reductions
-// (max of the value keys, then min of the expert ids holding it); lane j
-// keeps result j.  Weights: exp(l_j - l_0) normalised over
-// the k chosen (= softmax over all E renormalised over the k; the full
-// denominator cancels).
-__device__ void topk_token(const RouterArgs& a, int m, int lane, int* s_idx, float* s_w) {
+// Top-k of token m by one warp; lane l holds the keys of experts l + 32v.
+// Round j: the largest remaining value (redux max), then the lowest expert id
+// holding it (redux min); lane j keeps result j; the winning lane drops the
+// entry and every lane rescans its VPL keys (no divergent loop).  Weights:
+// exp(l_j - l_0) normalised over the k chosen = softmax over all E
+// renormalised over the k (the full denominator cancels).
+template <int VPL>
+__device__ void topk_token(const RouterArgs& a, int m, int lane) {
   const float* L = a.ws.logits + (size_t)m * a.E;
-  const int vpl = (a.E + 31) >> 5;
-  uint32_t key[32];
+  uint32_t key[VPL];
 #pragma unroll
-  for (int v = 0; v < 32; ++v) {
+  for (int v = 0; v < VPL; ++v) {
     const int e = v * 32 + lane;
-    key[v] = (v < vpl && e < a.E) ? ordered_key(__ldcg(L + e)) : 0u;
+    key[v] = e < a.E ? ordered_key(__ldcg(L + e)) : 0u;
   }
-  uint32_t taken = 0, bk = 0;
-  int bv = -1;
+  uint32_t best = 0;
+  int bv = 0;
 #pragma unroll
-  for (int v = 0; v < 32; ++v)
-    if (key[v] > bk) { bk = key[v]; bv = v; }
+  for (int v = 0; v < VPL; ++v)
+    if (key[v] > best) { best = key[v]; bv = v; }
 
   int my_idx = 0;
   float my_val = 0.f;
   for (int j = 0; j < a.K; ++j) {
-    // largest value, then the lowest expert id holding it
-    const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = (bv >= 0 && bk == top) ? (uint32_t)(bv * 32 + lane) : 0xffffffffu;
+    const uint32_t top = __reduce_max_sync(0xffffffffu, best);
+    const uint32_t cand = (best != 0u && best == top) ? (uint32_t)(bv * 32 + lane) : 0xffffffffu;
     uint32_t win = __reduce_min_sync(0xffffffffu, cand);
     if (win >= (uint32_t)a.E) {  // no candidate left: only a NaN logit pattern can cause it
       if (lane == 0) set_error(a.ws.status, kErrBadIndex);
@@ -120,14 +115,17 @@ __device__ void topk_token(const RouterArgs& a, int m, int lane, int* s_idx, flo
       my_idx = (int)win;
       my_val = key_value(top);
     }
-    if ((int)(win & 31u) == lane) {
-      taken |= 1u << (win >> 5);
-      bk = 0;
-      bv = -1;
+    const bool mine = (int)(win & 31u) == lane;
+    uint32_t nb = 0;
+    int nv = 0;
 #pragma unroll
-      for (int v = 0; v < 32; ++v)
-        if (!((taken >> v) & 1u) && key[v] > bk) { bk = key[v]; bv = v; }
+    for (int v = 0; v < VPL; ++v) {
+      const uint32_t kv = (mine && v == bv) ? 0u : key[v];
+      key[v] = kv;
+      if (kv > nb) { nb = kv; nv = v; }
     }
+    best = nb;
+    bv = nv;
   }
   const float v0 = __shfl_sync(0xffffffffu, my_val, 0);
   const float ex = lane < a.K ? expf(my_val - v0) : 0.f;
@@ -139,15 +137,23 @@ __device__ void topk_token(const RouterArgs& a, int m, int lane, int* s_idx, flo
     a.topk_idx[p] = my_idx;
     if (a.topk_w) a.topk_w[p] = w;
     a.ws.pair_w[p] = w;
-    s_idx[p] = my_idx;
-    s_w[p] = w;
   }
+}
+
+__device__ __forceinline__ void topk_dispatch(const RouterArgs& a, int m, int lane) {
+  if (a.E <= 32) topk_token<1>(a, m, lane);
+  else if (a.E <= 64) topk_token<2>(a, m, lane);
+  else if (a.E <= 128) topk_token<4>(a, m, lane);
+  else if (a.E <= 256) topk_token<8>(a, m, lane);
+  else if (a.E <= 512) topk_token<16>(a, m, lane);
+  else topk_token<32>(a, m, lane);
 }
 
 }  // namespace
 
 template <int CPL>
-__global__ void __launch_bounds__(kRouterThreads) router_topk_compact_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) uint4 xs[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterExpertsPerCta + warp;
   const bool has_row = e < a.E;
@@ -163,16 +169,45 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_compact_kernel(Rou
   }
   const float bias = (has_row && a.bias) ? __ldg(a.bias + e) : 0.f;
 
-  pdl_wait();                // x (and the workspace) now belong to this call
-  pdl_launch_dependents();   // the gate/up kernel may start its prologue
+  pdl_wait();               // x (and the workspace) now belong to this call
+  pdl_launch_dependents();  // the gate/up kernel may start its prologue
 
-  if (has_row) {
-    int m = 0;
-    for (; m + 2 <= a.M; m += 2) logits_tokens<CPL, 2>(a, w, m, e, bias, lane);
-    for (; m < a.M; ++m) logits_tokens<CPL, 1>(a, w, m, e, bias, lane);
+  const int hc = a.H >> 3;
+  const int nblk = (a.M + kRouterTokBlock - 1) / kRouterTokBlock;
+  stage_tokens(a, xs, 0);
+  for (int b = 0; b < nblk; ++b) {
+    if (b + 1 < nblk) {
+      stage_tokens(a, xs, b + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const int m0 = b * kRouterTokBlock;
+    const int tb = min(kRouterTokBlock, a.M - m0);
+    const uint4* xb = xs + (size_t)(b & 1) * kRouterTokBlock * hc + lane;
+    float s[kRouterTokBlock];
+#pragma unroll
+    for (int t = 0; t < kRouterTokBlock; ++t) s[t] = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+#pragma unroll
+      for (int t = 0; t < kRouterTokBlock; ++t)
+        if (t < tb) s[t] = dot8(w[c], xb[(size_t)t * hc + c * 32], s[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < kRouterTokBlock; ++t) {
+      if (t < tb) {
+        float v = s[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && has_row) a.ws.logits[(size_t)(m0 + t) * a.E + e] = v + bias;
+      }
+    }
+    __syncthreads();  // the buffer is refilled two blocks later
   }
 
-  // Last CTA to finish runs the top-k and the compaction.
+  // The last CTA to finish runs the top-k.
   __shared__ int s_last;
   __threadfence();
   __syncthreads();
@@ -180,98 +215,26 @@ __global__ void __launch_bounds__(kRouterThreads) router_topk_compact_kernel(Rou
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-
-  extern __shared__ int4 dyn_smem[];
-  const int NP = a.M * a.K;
-  int* s_idx = reinterpret_cast<int*>(dyn_smem);
-  float* s_w = reinterpret_cast<float*>(s_idx + NP);
-  int* s_cnt = reinterpret_cast<int*>(s_w + NP);
-  int* s_off = s_cnt + a.E;
-  int* s_run = s_off + a.E;
-
-  for (int m = warp; m < a.M; m += kRouterThreads / 32) topk_token(a, m, lane, s_idx, s_w);
-  for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
-    s_cnt[i] = 0;
-    s_run[i] = 0;
-  }
-  __syncthreads();
-  for (int p = threadIdx.x; p < NP; p += blockDim.x) atomicAdd(&s_cnt[s_idx[p]], 1);
-  __syncthreads();
-
-  if (warp == 0) {
-    // Bucket offsets (pairs), group offsets (<= 16 pairs per group) and the
-    // active-expert count: one exclusive scan over experts, lane-contiguous.
-    const int E = a.E;
-    const int per = (E + 31) >> 5;
-    const int e0 = lane * per, e1 = min(E, e0 + per);
-    int c_sum = 0, g_sum = 0, a_sum = 0;
-    for (int ex = e0; ex < e1; ++ex) {
-      const int c = s_cnt[ex];
-      c_sum += c;
-      g_sum += (c + kGroupTokens - 1) / kGroupTokens;
-      a_sum += c > 0;
-    }
-    int c_inc = c_sum, g_inc = g_sum, a_inc = a_sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int tc = __shfl_up_sync(0xffffffffu, c_inc, o);
-      const int tg = __shfl_up_sync(0xffffffffu, g_inc, o);
-      const int ta = __shfl_up_sync(0xffffffffu, a_inc, o);
-      if (lane >= o) {
-        c_inc += tc;
-        g_inc += tg;
-        a_inc += ta;
-      }
-    }
-    int c_off = c_inc - c_sum, g_off = g_inc - g_sum;
-    for (int ex = e0; ex < e1; ++ex) {
-      const int c = s_cnt[ex];
-      s_off[ex] = c_off;
-      for (int q = 0; q * kGroupTokens < c; ++q) {
-        const int g = g_off + q;
-        a.ws.grp_expert[g] = ex;
-        a.ws.grp_start[g] = c_off + q * kGroupTokens;
-        a.ws.grp_cnt[g] = min(kGroupTokens, c - q * kGroupTokens);
-      }
-      c_off += c;
-      g_off += (c + kGroupTokens - 1) / kGroupTokens;
-    }
-    if (lane == 31) {
-      *a.ws.n_groups = g_inc;
-      *a.ws.n_active = a_inc;
-    }
-    __syncwarp();
-    // Stable placement: position = bucket offset + pairs of the same expert
-    // with a smaller pair index.
-    for (int base = 0; base < NP; base += 32) {
-      const int p = base + lane;
-      const bool valid = p < NP;
-      const int ex = valid ? s_idx[p] : E + lane;  // sentinel never matches a real expert
-      const unsigned same = __match_any_sync(0xffffffffu, ex);
-      const int rank = __popc(same & ((1u << lane) - 1u));
-      int pos = 0;
-      if (valid) pos = s_off[ex] + s_run[ex] + rank;
-      __syncwarp();
-      if (valid) {
-        a.ws.pair_list[pos] = p;
-        if (rank == 0) s_run[ex] += __popc(same);
-      }
-      __syncwarp();
-    }
-  }
+  for (int m = warp; m < a.M; m += kRouterThreads / 32) topk_dispatch(a, m, lane);
+  __syncthreads();  // this CTA's topk_idx writes are visible to it
+  // token->expert compaction ("Two fusions and a retune", pair axis), built
+  // block-wide in shared memory (reusing the token buffer) and published
+  const SmemRouting rt = compact_routing(a.topk_idx, a.M * a.K, a.E, reinterpret_cast<int*>(xs),
+                                         a.ws.status);
+  publish_routing(rt, a.M * a.K, a.ws);
   if (threadIdx.x == 0) *a.ws.router_count = 0;  // ready for the next call
 }
 
 RouterKernel router_kernel_for(int cpl) {
   switch (cpl) {
-    case 1: return router_topk_compact_kernel<1>;
-    case 2: return router_topk_compact_kernel<2>;
-    case 4: return router_topk_compact_kernel<4>;
-    case 5: return router_topk_compact_kernel<5>;
-    case 8: return router_topk_compact_kernel<8>;
-    case 10: return router_topk_compact_kernel<10>;
-    case 12: return router_topk_compact_kernel<12>;
-    case 16: return router_topk_compact_kernel<16>;
+    case 1: return router_topk_kernel<1>;
+    case 2: return router_topk_kernel<2>;
+    case 4: return router_topk_kernel<4>;
+    case 5: return router_topk_kernel<5>;
+    case 8: return router_topk_kernel<8>;
+    case 10: return router_topk_kernel<10>;
+    case 12: return router_topk_kernel<12>;
+    case 16: return router_topk_kernel<16>;
     default: return nullptr;
   }
 }

@@ -81,6 +81,10 @@ class MoELayer:
 
     def forward_timed(self, x, out, topk_idx, events, stream=None):
         """Profiling launch: events = 4 torch.cuda.Event(enable_timing=True)."""
+        st = stream if stream is not None else torch.cuda.current_stream()
+        for e in events:
+            if not e.cuda_event:      # torch creates the CUDA event on first record
+                e.record(st)
         arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         rc = N.lib().moe_forward_timed(self._h, _ptr(x), _ptr(out), _ptr(topk_idx), x.shape[0],
                                        _stream_ptr(stream), arr)
