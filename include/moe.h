@@ -196,6 +196,42 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
                      int32_t* grp_expert, int32_t* grp_start, int32_t* grp_cnt,
                      int32_t* pair_list, float* pair_w, int cap);
 
+/*
+ * moe_route_static -- the router alone (gate matvec + softmax top-k with
+ * renormalisation) for callers that cannot allocate device memory.
+ *
+ * The source post has no counterpart: this is a library service.  Callers
+ * that cannot call cudaMalloc (code running while someone else captures a
+ * CUDA graph, allocators that forbid outside allocations, paths that must not
+ * risk an allocation failure or the synchronisation an allocation can imply)
+ * get the same routing as moe_forward without a handle: the call allocates
+ * nothing.  Its scratch (logits, an arrival counter, the compaction) is one
+ * fixed array inside the library image, 76,032 bytes, which every GPU that
+ * loads the library holds until the process exits.
+ *   hidden, n_experts, topk   as for moe_create.
+ *   x          device bf16 [M][hidden], 16-byte aligned.
+ *   w_router   device bf16 [n_experts][hidden], 16-byte aligned; read in
+ *              place (not copied), caller-owned.
+ *   bias       device fp32 [n_experts] added to the logits, or NULL.
+ *   M          0 <= M <= 16 (the scratch is sized for 16 tokens).
+ *   topk_idx   device int32 [M][topk]: experts by descending logit, ties to
+ *              the lower id (same values as moe_forward's topk_idx).
+ *   topk_w     NULL or device fp32 [M][topk]: the renormalised weights.
+ *   stream     CUDA stream.
+ * The first call on a device resolves the array's device address (a one-time
+ * set-up); make that first call before any stream capture.  A call may raise
+ * the router kernel's shared-memory limit, never lower it.  Every call on a device uses the same array and it keeps
+ * the last call's contents (the counter that must start at zero is cleared by
+ * each call on its stream), so calls whose work can overlap on the GPU --
+ * different streams without ordering -- race.  Returns MOE_ERR_UNSUPPORTED
+ * (with a moe_last_error() message) for M > 16 or sizes outside the limits,
+ * MOE_ERR_INVALID_ARG for bad pointers, MOE_ERR_CUDA if set-up or the launch
+ * fails.
+ */
+int moe_route_static(int hidden, int n_experts, int topk, const void* x,
+                     const void* w_router, const float* bias, int M,
+                     int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
 /* moe_destroy -- synchronises the handle's device, frees everything.
  * NULL is a no-op. */
 void moe_destroy(moe_layer_t* h);

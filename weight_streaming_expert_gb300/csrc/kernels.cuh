@@ -58,4 +58,7 @@ void pack_gate_up(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int I, in
                   cudaStream_t s);
 void pack_down(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int H, int I, cudaStream_t s);
 
+// Set the calling thread's moe_last_error() text (moe_api.cu).
+void set_last_error_text(const char* text);
+
 }  // namespace wse

@@ -192,6 +192,8 @@ int check_forward_args(moe_layer* h, const void* x, const void* out, const int32
 
 }  // namespace
 
+void wse::set_last_error_text(const char* text) { g_last_error = text ? text : ""; }
+
 extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
