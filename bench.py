@@ -66,7 +66,7 @@ def source_hash(paths):
 
 
 GATEUP_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
-                  for f in ("expert_gateup.cu", "common.cuh", "kernels.cuh")]
+                  for f in ("expert_gateup.cu", "compaction.cuh", "common.cuh", "kernels.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gateup_traffic.json")
 
 
@@ -536,7 +536,8 @@ def main(argv=None):
     ap.add_argument("--pool", type=int, default=64, help="distinct token batches cycled")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--all-m", action="store_true", help="also time M=1 and M=16 (Zipf) in the same run")
+    ap.add_argument("--no-all-m", dest="all_m", action="store_false",
+                    help="skip the M=1 and M=16 (Zipf) side measurements")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle timing")
     ap.add_argument("--sweep", action="store_true")
     args = ap.parse_args(argv)
