@@ -51,12 +51,6 @@ def algorithmic_bytes(hidden, n_experts, topk, inter, M, n_active):
     return (n_active * expert + n_experts * hidden * 2 + 2 * M * hidden * 2 + M * topk * 4)
 
 
-def gateup_bytes(hidden, inter, M, n_active, topk):
-    """Algorithmic bytes of the gate/up kernel: its weights once per distinct
-    expert, x in, the activated rows h out."""
-    return n_active * 2 * inter * hidden * 2 + M * hidden * 2 + M * topk * inter * 2
-
-
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -65,9 +59,10 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-GATEUP_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
-                  for f in ("expert_gateup.cu", "compaction.cuh", "common.cuh", "kernels.cuh")]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gateup_traffic.json")
+LAYER_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
+                 for f in ("layer_kernel.cuh", "routing.cuh", "common.cuh", "kernels.cuh",
+                           "layer_kernel_a.cu", "layer_kernel_b.cu")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "layer_traffic.json")
 
 
 def measured_peaks():
@@ -273,14 +268,14 @@ def time_graph(wkl, steps, warmup, pg, graph_len=64, sample_clocks=False, gpu_in
     return max_over_ranks(pg, ms), active, clocks
 
 
-def time_kernels(wkl, calls):
-    """Per-kernel durations (ms): the calls are launched without PDL with an
-    event between consecutive kernels, captured into one CUDA graph and
+def time_kernel_alone(wkl, calls):
+    """Layer-kernel durations (ms) without PDL overlap: each call is launched
+    without PDL between two events, all captured into one CUDA graph and
     replayed, so no host gap sits between the events."""
     import torch
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(calls)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(calls)]
     with torch.cuda.stream(s):
         for ev in evs:
             for e in ev:
@@ -297,11 +292,41 @@ def time_kernels(wkl, calls):
     torch.cuda.synchronize()
     g.replay()
     torch.cuda.synchronize()
-    t = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(3)] for ev in evs])
-    active = []
-    for c in range(calls):
-        active.append(int(torch.unique(wkl.idxs[c % len(wkl.xs)]).numel()))
-    return t, active
+    return np.array([ev[0].elapsed_time(ev[1]) for ev in evs])
+
+
+# trace slots (moe_read_trace): 0 wait passed, 1 matvec done, 2 grid barrier,
+# 3 routing ready, 4 first gate/up tile, 5 gate/up left, 6 h rows of all CTAs,
+# 7 down left, 8 combine done, 9 last gate/up issue, 10 down prefetch issued
+def phase_breakdown(wkl, reps=2):
+    """Phase timeline of the layer kernel inside a PDL-chained graph: every
+    layer's last call of a traced graph, times relative to that call's first
+    CTA passing its dependency wait (us; median over the calls read)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    n = reps * len(wkl.layers)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for c in range(n):
+                i = c % len(wkl.xs)
+                wkl.layers[c % len(wkl.layers)](wkl.xs[i], out=wkl.outs[i], topk_idx=wkl.idxs[i], stream=s,
+                                                 trace=True)
+    g.replay()
+    torch.cuda.synchronize()
+    rows = []
+    for layer in wkl.layers:
+        t = layer.read_trace().astype(np.float64)
+        t0 = t[:, 0].min()
+        r = (t - t0) / 1000.0
+        rows.append({
+            "matvec_done": r[:, 1].max(), "grid_barrier": r[:, 2].max(), "routing_ready": r[:, 3].max(),
+            "first_gateup_tile_median": float(np.median(r[:, 4])), "gateup_end_min": r[:, 5].min(),
+            "gateup_end_max": r[:, 5].max(), "h_ready": r[:, 6].max(), "down_end_min": r[:, 7].min(),
+            "down_end_max": r[:, 7].max(), "combine_end": r[:, 8].max(),
+            "gateup_tiles_per_cta_min": float(t[:, 11].min()), "gateup_tiles_per_cta_max": float(t[:, 11].max())})
+    return {k: round(float(np.median([r[k] for r in rows])), 3) for k in rows[0]}
 
 
 def time_e2e(wkl, steps):
@@ -398,16 +423,14 @@ def run_ours(args):
     us = ms * 1000.0
     gbs = bytes_call / (us * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
-    # per-kernel durations (eager launches, events between kernels)
-    kt, kact = time_kernels(wkl, min(256, max(16, args.steps)))
-    kt_mean = kt.mean(axis=0) * 1000.0       # us: router, gate/up, down
-    gu_bytes = float(np.mean([gateup_bytes(shape.hidden, shape.inter, M, a, shape.topk) for a in kact]))
-    gu_gbs = gu_bytes / (kt_mean[1] * 1e-6) / 1e9
+    # the layer kernel alone (no PDL overlap with its neighbours) and its phases
+    alone_us = float(time_kernel_alone(wkl, min(256, max(16, args.steps))).mean() * 1000.0)
+    phases = phase_breakdown(wkl)
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
-        if tr.get("source_hash") == source_hash(GATEUP_SOURCES) and tr.get("M") == M:
+        if tr.get("source_hash") == source_hash(LAYER_SOURCES) and tr.get("M") == M:
             traffic = tr.get("bytes_per_launch")
     e2e_us, h2d, d2h = (None, 0, 0)
     if not args.no_e2e:
@@ -451,15 +474,17 @@ def run_ours(args):
             "achieved_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
             "peak_gbs": peak, "peak_kind": peak_kind,
             "mean_active_experts": round(mean_active, 2), "algorithmic_bytes_per_call": int(bytes_call),
-            "kernel_us": {"router_topk_compact": round(kt_mean[0], 3), "gateup_swiglu": round(kt_mean[1], 3),
-                          "down_combine": round(kt_mean[2], 3), "timing": "graph replay, no PDL, events between kernels"},
-            "roofline": {"bound": "hbm", "kernel": "gateup_swiglu", "achieved": round(gu_gbs, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(gu_gbs / peak, 4), "traffic": traffic,
-                         "algorithmic_bytes_per_launch": int(gu_bytes), "peak_kind": peak_kind},
+            "kernel_us": {"moe_layer_kernel_in_chain": round(us, 3), "moe_layer_kernel_alone": round(alone_us, 3),
+                          "alone_timing": "graph replay, no PDL, events around each launch"},
+            "phases_us": phases,
+            "roofline": {"bound": "hbm", "kernel": "moe_layer_kernel", "achieved": round(gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": int(bytes_call), "peak_kind": peak_kind,
+                         "launch_duration": "timed-region mean per launch (one launch per call, PDL-chained)"},
             "cpu_baseline": cpu,
             "e2e": None if e2e_us is None else {"value": round(e2e_us, 3), "unit": UNIT,
                                                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": args.steps,
             "clocks": clocks,
         }
         if by_m:
@@ -511,16 +536,13 @@ def run_sweep(args):
         for M in (1, 2, 4, 6, 8, 16, 32, 64):
             wkl.new_pool(M, args.pool)
             ms, active, _ = time_graph(wkl, args.steps, args.warmup, None)
-            kt, kact = time_kernels(wkl, 64)
             b = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, float(np.mean(active)))
             gb = b / (ms * 1e-3) / 1e9
-            gu = float(np.mean([gateup_bytes(shape.hidden, shape.inter, M, a, shape.topk) for a in kact]))
             print(json.dumps({"sweep": True, "M": M, "routing": "zipf" if zipf else "uniform",
                               "us_per_call": round(ms * 1000, 3), "achieved_gbs": round(gb, 1),
                               "frac_of_peak": round(gb / peak, 4), "peak_kind": peak_kind,
                               "mean_active_experts": round(float(np.mean(active)), 2),
-                              "kernel_us": [round(v, 3) for v in (kt.mean(axis=0) * 1000)],
-                              "gateup_gbs": round(gu / (kt.mean(axis=0)[1] * 1e-3) / 1e9, 1)}), flush=True)
+                              "phases_us": phase_breakdown(wkl, reps=1)}), flush=True)
     wkl.close()
 
 

@@ -5,9 +5,12 @@
  *   router gate matvec -> softmax top-k with renormalisation -> on-device
  *   token->expert compaction -> fused gate/up GEMV + SwiGLU -> down GEMV with
  *   the routing-weighted combine in its epilogue.
- * Three kernels, chained with Programmatic Dependent Launch, capturable in
- * one CUDA graph.  No host synchronisation, no allocation and no
- * device->host copy happens inside the forward call.
+ * One persistent kernel (one CTA per SM, grid-wide barriers inside), chained
+ * to the previous work on the stream with Programmatic Dependent Launch and
+ * capturable in a CUDA graph.  No host synchronisation, no allocation and no
+ * device->host copy happens inside the forward call.  The kernel needs the
+ * whole GPU: every one of its CTAs must be resident at once (they are, one
+ * per SM, when no other work holds an SM for the kernel's whole duration).
  *
  * Source of the method (page title and section):
  *   "How Ling-3.0-flash reduces batch 1 decoding latency by 54% on 4
@@ -69,10 +72,12 @@ typedef enum {
 #define MOE_MAX_TOKENS 64
 
 /* Flags for moe_forward_ex. */
-#define MOE_FWD_NO_PDL 0x1u /* launch the three kernels without PDL        */
+#define MOE_FWD_NO_PDL 0x1u /* launch without PDL                            */
 #define MOE_FWD_GRAPH 0x2u  /* replay a per-(handle, M) CUDA graph instead of
-                               three launches; the graph is captured on first
-                               use and updated when the pointers change       */
+                               a launch; the graph is captured on first use
+                               and updated when the pointers change           */
+#define MOE_FWD_TRACE 0x4u  /* record per-CTA phase timestamps of this call
+                               (read with moe_read_trace); same results       */
 
 /*
  * moe_create -- build a layer handle from bf16 weights.
@@ -85,6 +90,7 @@ typedef enum {
  *   inter      I: expert intermediate width, one of {128, 256, 512}.
  *   w_router   device bf16 [E][H], row e = router row of expert e
  *              (the hidden -> n_experts mapping, stored one row per expert).
+ *              All three weight pointers must be 16-byte aligned.
  *   w_gate_up  device bf16 [E][2I][H]; rows [0,I) are the gate projection,
  *              rows [I,2I) the up projection of each expert.
  *   w_down     device bf16 [E][H][I]; the down projection of each expert.
@@ -135,12 +141,11 @@ int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx,
                    float* topk_w, int M, moe_stream_t stream, unsigned flags);
 
 /*
- * moe_forward_timed -- profiling variant: plain launches without PDL, with
- * ev[0] recorded before the router kernel, ev[1] after it, ev[2] after the
- * gate/up kernel and ev[3] after the down/combine kernel, all on `stream`.
- * ev must point to 4 valid events.  Same results as moe_forward.  Under
+ * moe_forward_timed -- profiling variant: a plain launch without PDL, with
+ * ev[0] recorded before the layer kernel and ev[1] after it, on `stream`.
+ * ev must point to 2 valid events.  Same results as moe_forward.  Under
  * stream capture the records become event nodes of the graph, so a replay
- * times the kernels with no host gap between them.
+ * times the kernel with no host gap around it.
  */
 int moe_forward_timed(moe_layer_t* h, const void* x, void* out,
                       int32_t* topk_idx, int M, moe_stream_t stream,
@@ -158,8 +163,10 @@ int moe_set_router_bias(moe_layer_t* h, const float* bias);
 /*
  * moe_get_status -- synchronises the device, then returns and clears the
  * handle's sticky device error word: MOE_OK, or MOE_ERR_DEVICE_TIMEOUT if a
- * bounded wait inside a kernel gave up (the outputs of that call are then
- * undefined).  Not for the hot path.
+ * bounded wait inside the kernel gave up (a staging wait, or a grid-wide
+ * wait when not every CTA could be resident), after which the outputs of
+ * that call are undefined; moe_last_error() then names the first wait that
+ * gave up.  Not for the hot path.
  */
 int moe_get_status(moe_layer_t* h);
 
@@ -168,13 +175,15 @@ typedef struct {
   int hidden, n_experts, topk, inter;
   int max_tokens;          /* MOE_MAX_TOKENS */
   int n_sms;               /* SMs of the device the handle lives on */
-  int gateup_stages;       /* shared-memory ring depth of the gate/up kernel */
-  int down_stages;         /* ring depth of the down/combine kernel */
+  int gateup_stages;       /* shared-memory ring depth of the gate/up phase */
+  int down_stages;         /* shared-memory stages of the down phase */
   int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 rows x H) */
   int down_tile_bytes;     /* bytes of one down weight tile (8 rows x I) */
   size_t weight_bytes;     /* device bytes held for the weights */
   size_t workspace_bytes;  /* device bytes held for the workspace */
-  int kernels_per_forward; /* kernel launches per forward call */
+  int kernels_per_forward; /* kernel launches per forward call (1) */
+  int router_split;        /* hidden-dim split of the router matvec units */
+  size_t smem_bytes;       /* dynamic shared memory per CTA at M = 64 */
 } moe_info_t;
 
 int moe_get_info(const moe_layer_t* h, moe_info_t* out);
@@ -197,6 +206,25 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
                      int32_t* pair_list, float* pair_w, int cap);
 
 /*
+ * moe_read_trace -- copy the phase timestamps of the last call made with
+ * MOE_FWD_TRACE (synchronises the device; profiling aid).
+ *   out   host uint64 [cap]: for CTA c, slots [16c, 16c + 16) hold
+ *         %globaltimer values in ns: 0 dependency wait passed, 1 router
+ *         matvec done, 2 grid barrier passed, 3 top-k + compaction done,
+ *         4 first gate/up tile consumed, 5 gate/up loop left, 6 every CTA's
+ *         SwiGLU rows written, 7 down loop left, 8 combine done, 9 producer
+ *         issued its last gate/up tile, 10 producer issued its last
+ *         down tile, 12 top-k done, 13 compaction done, 14 first down
+ *         tile consumed, 15 slab arrivals complete; slot 11 holds the
+ *         CTA's gate/up tile COUNT.  Slots of phases a CTA did not reach
+ *         keep older values.
+ * Returns the number of values written (min(cap, 16 x SMs)), or on error
+ * the negated moe_status_t (a positive status could not be told apart from a
+ * count).
+ */
+int moe_read_trace(moe_layer_t* h, uint64_t* out, int cap);
+
+/*
  * moe_route_static -- the router alone (gate matvec + softmax top-k with
  * renormalisation) for callers that cannot allocate device memory.
  *
@@ -205,9 +233,11 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
  * CUDA graph, allocators that forbid outside allocations, paths that must not
  * risk an allocation failure or the synchronisation an allocation can imply)
  * get the same routing as moe_forward without a handle: the call allocates
- * nothing.  Its scratch (logits, an arrival counter, the compaction) is one
- * fixed array inside the library image, 76,032 bytes, which every GPU that
- * loads the library holds until the process exits.
+ * nothing.  Its scratch (partial logits, an arrival counter, a status word)
+ * is one fixed array inside the library image, 78,080 bytes, which every GPU
+ * that loads the library holds until the process exits.  Its arithmetic is
+ * moe_forward's own router (same matvec split and summation order, same
+ * top-k), so both give the same routing for the same x.
  *   hidden, n_experts, topk   as for moe_create.
  *   x          device bf16 [M][hidden], 16-byte aligned.
  *   w_router   device bf16 [n_experts][hidden], 16-byte aligned; read in
@@ -219,8 +249,8 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
  *   topk_w     NULL or device fp32 [M][topk]: the renormalised weights.
  *   stream     CUDA stream.
  * The first call on a device resolves the array's device address (a one-time
- * set-up); make that first call before any stream capture.  A call may raise
- * the router kernel's shared-memory limit, never lower it.  Every call on a device uses the same array and it keeps
+ * set-up); make that first call before any stream capture.  Every call on a
+ * device uses the same array and it keeps
  * the last call's contents (the counter that must start at zero is cleared by
  * each call on its stream), so calls whose work can overlap on the GPU --
  * different streams without ordering -- race.  Returns MOE_ERR_UNSUPPORTED

@@ -41,9 +41,12 @@ def test_expert_traffic_matches_the_post():
     assert abs(experts - val) <= tol * val
 
 
-def test_gateup_bytes_are_two_thirds_of_expert_bytes():
-    g = bench.gateup_bytes(2560, 512, M=6, n_active=46, topk=8) - 6 * 2560 * 2 - 6 * 8 * 512 * 2
-    assert 3 * g == 2 * 46 * 3 * 2560 * 512 * 2
+def test_call_bytes_count_router_and_io_once():
+    # no expert chosen: the router weight once, x in, out out, the indices out
+    base = bench.algorithmic_bytes(2560, 512, 8, 512, M=6, n_active=0)
+    assert base == 512 * 2560 * 2 + 2 * 6 * 2560 * 2 + 6 * 8 * 4
+    # each distinct expert adds its gate, up and down weights exactly once
+    assert bench.algorithmic_bytes(2560, 512, 8, 512, M=6, n_active=46) - base == 46 * 3 * 2560 * 512 * 2
 
 
 def test_layer_count_keeps_l2_cold():

@@ -378,8 +378,8 @@ def test_timed_launch_matches(ling):
     ref, ridx = layer(x)
     out = torch.empty_like(x)
     idx = torch.empty_like(ridx)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     layer.forward_timed(x, out, idx, ev)
     torch.cuda.synchronize()
     assert torch.equal(out, ref) and torch.equal(idx, ridx)
-    assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(3))
+    assert ev[0].elapsed_time(ev[1]) > 0

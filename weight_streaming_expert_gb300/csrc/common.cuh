@@ -1,6 +1,6 @@
-// common.cuh -- sm_103a building blocks shared by the layer's kernels:
-// mbarrier + bulk-copy (TMA) staging, Programmatic Dependent Launch control,
-// the bf16 tensor-core MMA, and the workspace shared by the three kernels.
+// common.cuh -- sm_103a building blocks of the layer kernel: mbarrier +
+// bulk-copy (TMA) staging, Programmatic Dependent Launch control, the bf16
+// tensor-core MMA, and the device workspace of a layer handle.
 #pragma once
 
 #include <cstdint>
@@ -15,14 +15,29 @@ constexpr int kMaxExperts = 1024;     // E
 constexpr int kMaxPairs = kMaxTokens * kMaxTopk;
 constexpr int kGroupTokens = 16;      // pairs per compaction group (one m16 / 2 x n8 tile)
 constexpr int kConsumerWarps = 8;
-constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
-constexpr int kRouterThreads = 256;   // 8 warps, one expert row each
-constexpr int kRouterExpertsPerCta = kRouterThreads / 32;
-constexpr int kGateUpTileRows = 8;    // 4 gate rows interleaved with 4 up rows
-constexpr int kDownTileRows = 8;     // 8 output rows (n8) x I per down tile
-constexpr int kMaxGateUpStages = 7;   // < kConsumerWarps: see the reduction-slot argument
-constexpr int kMaxDownStages = 24;    // a multiple of kConsumerWarps: each stage has one owner warp
+constexpr int kProducerWarp = kConsumerWarps;      // warp 8: stages every weight tile
+constexpr int kPublisherWarp = kConsumerWarps + 1; // warp 9: grid-wide arrivals and readiness
+constexpr int kExpertThreads = (kConsumerWarps + 2) * 32;
+constexpr int kGateUpTileRows = 8;    // 4 gate rows interleaved with their 4 up rows
+constexpr int kDownTileRows = 8;      // 8 output rows (n8) x I per down tile
+constexpr int kMaxGateUpStages = 7;   // < 8 reduction slots: see the reduction-slot argument
+constexpr int kMaxDownStages = 8;     // down stages of 8 slabs (one per consumer warp)
+constexpr int kMaxDownChunks = 16;    // 32-wide k chunks of a down row: I <= 512
 constexpr uint32_t kBulkChunk = 16384;  // bytes per cp.async.bulk
+constexpr int kTraceSlots = 32;       // per-CTA phase timestamps of a traced call
+
+// Grid-wide synchronisation words (unsigned, 128 bytes apart).  The 64-bit
+// counts are never reset: each call adds exactly one arrival per CTA to each
+// of the last two and two (the two barriers) to the first, so the barrier
+// after the router tells every CTA the call's index and every later target.
+enum : int {
+  kSyncCount = 0,         // 64-bit: arrivals at the grid barriers (after the router, before the combine)
+  kSyncGateUpNext = 32,   // next gate/up tile of the dynamically shared tail
+  kSyncDownNext = 64,     // next down super tile of the dynamically shared tail
+  kSyncStaticDone = 96,   // 64-bit: CTAs whose statically assigned gate/up tiles are reduced
+  kSyncGateUpDone = 128,  // 64-bit: CTAs whose gate/up tiles are all reduced
+  kSyncWords = 160,
+};
 
 // A bounded wait gives up after this long (the kernels run for microseconds;
 // reaching it means a bug, never a slow call).
@@ -33,25 +48,26 @@ enum : int {
   kErrTimeoutFull = 1,    // consumer waited too long for a staged tile
   kErrTimeoutEmpty = 2,   // producer waited too long for a free stage
   kErrTimeoutReduce = 4,  // gate/up reducer waited too long for partials
-  kErrBadIndex = 8,       // a routing index read from the workspace was out of range
+  kErrBadIndex = 8,       // the top-k found no candidate (cannot happen while k <= E)
+  kErrTimeoutGrid = 16,   // a grid-wide wait (barrier, h rows, slab arrivals) ran out
 };
 
 // Device workspace of one layer handle (all device pointers).
 struct Workspace {
-  int* status;        // [1] sticky error bits
-  unsigned long long* diag;  // [4] first timeout: where, elapsed ns, raw barrier word, spare
-  int* router_count;  // [1] CTAs of the router kernel that finished (last-CTA-done)
-  int* n_groups;      // [1] compaction groups published for this call (router's last CTA)
-  int* n_active;      // [1] distinct experts this call
-  int* grp_expert;    // [kMaxPairs]
-  int* grp_start;     // [kMaxPairs] first sorted position of the group
-  int* grp_cnt;       // [kMaxPairs] pairs in the group (1..16)
-  int* pair_list;     // [kMaxPairs] pair id (token*k + slot) at each sorted position
-  float* pair_w;      // [kMaxPairs] routing weight by pair id
-  float* logits;      // [kMaxTokens][E]
-  __nv_bfloat16* h;   // [kMaxPairs][I] activated rows, sorted-position order
-  float* y;           // [kMaxPairs][H] weighted down-projection rows, by pair id
-  int* slab_count;    // [H/8] groups finished per 8-row output slab
+  int* status;               // [1] sticky error bits
+  unsigned long long* diag;  // [4] first timeout: where, elapsed ns, raw barrier word, thread/grid
+  unsigned* sync;            // [kSyncWords] grid-wide counters, see above
+  float* part;               // [ks][kMaxTokens][E] partial router logits
+  int* n_groups;             // [1] copy of the call's compaction (inspection only)
+  int* n_active;             // [1]
+  int* grp_expert;           // [kMaxPairs]
+  int* grp_start;            // [kMaxPairs] first sorted position of the group
+  int* grp_cnt;              // [kMaxPairs] pairs in the group (1..16)
+  int* pair_list;            // [kMaxPairs] pair id (token*k + slot) at each sorted position
+  float* pair_w;             // [kMaxPairs] routing weight by pair id
+  __nv_bfloat16* h;          // [kMaxPairs][I] SwiGLU rows, sorted-position order
+  float* y;                  // [kMaxPairs][H] weighted down-projection rows, by pair id
+  unsigned long long* trace; // [grid][kTraceSlots] phase timestamps (traced calls)
 };
 
 // ------------------------------------------------------------- PTX -----
@@ -124,6 +140,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Warp-uniform bounded wait: every lane waits and the lanes agree on the
+// outcome by vote, so a timeout never splits the warp before a .aligned
+// instruction (mma.sync) or a __syncwarp().
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned long long* waited) {
+  const bool ok = mbar_wait(bar, parity, waited);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Order this thread's earlier generic-proxy shared-memory accesses before its
 // later async-proxy (bulk copy) accesses -- needed before refilling a stage
 // that was just read with ordinary loads.
@@ -170,8 +194,9 @@ __device__ __forceinline__ unsigned long long mbar_raw(uint32_t bar) {
   return v;
 }
 
-// Record the first bounded-wait timeout of a call (kernel id 1..3, wait kind
-// = the status bit, CTA, loop index, ring depth) and its evidence.
+// Record the first bounded-wait timeout of a call (phase 1 router / 2
+// gate-up / 3 down, wait kind = the status bit, CTA, loop index, ring depth)
+// and its evidence.
 __device__ __forceinline__ void record_timeout(const Workspace& ws, int kernel, int kind, int j,
                                                int stages, uint32_t bar, unsigned long long waited) {
   const unsigned long long where = ((unsigned long long)kernel << 56) |

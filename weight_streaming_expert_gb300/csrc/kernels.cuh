@@ -1,57 +1,45 @@
-// kernels.cuh -- argument blocks and launch-side declarations of the layer's
-// three forward kernels and the create-time weight re-layout kernels.
+// kernels.cuh -- argument block and launch-side declarations of the layer
+// kernel, the allocation-free routing kernel and the create-time weight
+// re-layout.
 #pragma once
+
+#include <cuda_runtime.h>
 
 #include "common.cuh"
 
 namespace wse {
 
-struct RouterArgs {
+struct LayerArgs {
   const __nv_bfloat16* x;         // [M][H]
-  const __nv_bfloat16* w_router;  // [E][H]
+  const __nv_bfloat16* w_router;  // [E][H] (caller layout)
   const float* bias;              // [E] or nullptr
-  int M, H, E, K;
+  const uint8_t* w_gate_up;       // packed gate/up tiles, see pack.cu
+  const uint8_t* w_down;          // packed down tiles, see pack.cu
+  __nv_bfloat16* out;             // [M][H]
   int32_t* topk_idx;              // [M][K] caller output
   float* topk_w;                  // [M][K] caller output or nullptr
+  int M, H, E, K, I;
+  int ks;                         // hidden-dim split of the router matvec
+  int gu_stages;                  // gate/up ring depth
+  int d_stages;                   // down stages, a multiple of 8
+  uint32_t gu_tile;               // 8 rows x H x 2 bytes
+  uint32_t d_tile;                // 8 rows x I x 2 bytes
+  uint32_t ring_bytes;            // max(gu_stages*gu_tile + reduction area, d_stages*d_tile)
+  int trace;                      // record phase timestamps
+  // per down stage: bit s = the stage's bytes overlap gate/up stage s, bit
+  // 31 = they overlap the reduction area (a pure function of the four sizes
+  // above, computed at create)
+  uint32_t d_need[kMaxDownStages];
   Workspace ws;
 };
 
-struct GateUpArgs {
-  const uint8_t* w_gate_up;  // packed gate/up tiles, see pack.cu
-  const __nv_bfloat16* x;    // [M][H]
-  const int32_t* topk_idx;   // [M][K] the router's expert ids
-  int M, H, I, K, E;
-  int stages;                // ring depth
-  uint32_t tile_bytes;       // 8 rows x H x 2
-  Workspace ws;
-};
-
-struct DownArgs {
-  const uint8_t* w_down;     // packed down tiles, see pack.cu
-  __nv_bfloat16* out;        // [M][H]
-  const int32_t* topk_idx;   // [M][K] the router's expert ids
-  int M, H, I, K, E;
-  int stages;
-  uint32_t tile_bytes;       // 16 rows x I x 2
-  Workspace ws;
-};
-
-// Router + top-k: grid ceil(E/8) x 256 threads, dynamic smem
-// router_smem_bytes(M, H, K, E).  CPL = H/256 (16-byte chunks of a row per lane).
-using RouterKernel = void (*)(RouterArgs);
-RouterKernel router_kernel_for(int cpl);
-size_t router_smem_bytes(int M, int H, int K, int E);
-
-// Gate/up + SwiGLU: grid = #SMs x kExpertThreads.  KPW = H/256.
-using GateUpKernel = void (*)(GateUpArgs);
-GateUpKernel gateup_kernel_for(int kpw);
-size_t gateup_smem_bytes(int stages, uint32_t tile_bytes, int NP, int E);
-
-// Down + combine: grid = #SMs x kDownThreadsPerCta.  KS = I/16.
-constexpr int kDownThreadsPerCta = kConsumerWarps * 32;
-using DownKernel = void (*)(DownArgs);
-DownKernel down_kernel_for(int ks);
-size_t down_smem_bytes(int stages, uint32_t tile_bytes, int NP, int E, int H);
+// The layer kernel: grid = #SMs x kExpertThreads, dynamic shared memory
+// layer_smem_bytes(ring_bytes, M*K, E).  KPW = H/256.
+using LayerKernel = void (*)(LayerArgs);
+LayerKernel layer_kernel_for(int kpw);
+size_t layer_smem_bytes(uint32_t ring_bytes, int NP, int E);
+// Bytes of the reduction area that follows the gate/up stages.
+uint32_t layer_reduction_bytes();
 
 // Create-time re-layout (pack.cu).
 void pack_gate_up(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int I, int H,

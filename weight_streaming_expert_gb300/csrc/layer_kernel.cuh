@@ -1,0 +1,668 @@
+// layer_kernel.cuh -- one routed-MoE layer call as ONE persistent kernel:
+// router matvec -> grid barrier -> softmax top-k + compaction -> gate/up
+// GEMV with SwiGLU -> down GEMV with the weighted combine.
+//
+// Method (page "How Ling-3.0-flash reduces batch 1 decoding latency by 54%
+// on 4 Blackwell GPUs"):
+//  * "Two kinds of idle": at small batch the critical path is the cold read
+//    of the activated expert weights plus the launch floor; a routed layer
+//    per step reads the router gate (2.6 MB at hidden 2560 x 512 experts)
+//    and every activated expert's gate/up and down weights.
+//  * "Economics of speculation at batch 1": verifying several tokens reads
+//    the same weights as verifying one, so each activated expert is
+//    streamed from HBM once for all of its tokens.
+//  * "Two fusions and a retune": SwiGLU is folded into the up-projection
+//    epilogue (fp32, one rounding to bf16, gate/up rows interleaved at load);
+//    the token->expert alignment runs on the device on the pair axis.
+//  * "PDL: the latency floor of stacked small kernels": producer-independent
+//    loads go before the dependency wait; the small-M combine is an fp32 sum
+//    with a single final cast (scale 1 here).
+//
+// GB300 design.  Grid = one CTA per SM (all resident: every CTA needs most of
+// the SM's shared memory), 8 consumer warps, 1 producer warp (stages every
+// weight tile) and 1 publisher warp (grid-wide arrivals and waits, so that
+// no fence or atomic round trip ever stalls a thread that streams).
+//  1. Prologue, before the dependency wait: barriers, the CTA's slice of
+//     the router weight into registers.
+//  2. Router matvec on the tensor cores (routing.cuh), fp32 partial logits
+//     to the workspace, then a grid-wide barrier (bounded spin).
+//  3. EVERY CTA computes the top-k of all tokens and the compaction itself
+//     (shared memory only): nothing is published and re-read, no second
+//     launch, no last-CTA hand-off.  The results are bitwise equal in all
+//     CTAs (same inputs, same code), so they agree on every position.
+//  4. Gate/up: (group, 8-row) tiles of 8 weight rows x H, staged by the
+//     producer with bulk copies into a ring of mbarrier-guarded stages.
+//     The tiles of the first 3/4 of the groups are split statically, the
+//     rest are taken one at a time from a global counter, so SMs that stream
+//     faster take more (the per-SM rate differs by several per cent).  The producer writes each
+//     stage's tile id and signals it before the copy lands, so consumers
+//     fetch the group's token rows early.  Eight warps split H; a rotating
+//     reducer warp sums their partials in a fixed order and applies SwiGLU.
+//  5. Down: (group, 64-output-row) super tiles = 8 slabs of 8 rows x I,
+//     one slab per consumer warp, staged the same way (the same producer,
+//     the same 3/4 static + dynamic tail split, the same early tile ids).
+//     The producer puts the first down super tiles into ring bytes as soon
+//     as the gate/up tiles there are consumed for the last time -- HBM does
+//     not drain between the two GEMVs.  No grid-wide barrier sits between
+//     the GEMVs either: a down tile needs only its own group's h rows.
+//     Every CTA's publisher counts it in when its statically split gate/up
+//     tiles are reduced, and again when all of them are; a group whose
+//     gate/up tiles all lie in the static share is ready once every CTA is
+//     counted in the first, any other group once in the second.  The
+//     publisher turns the two grid-wide counts into two shared-memory
+//     barriers; the producer waits on the one a tile's group needs before it
+//     hands the tile id to the consumers (its copy is already in flight).
+//     The static down share holds (nearly) only early groups, so in practice
+//     nothing waits.
+//  6. Combine: once every CTA's weighted rows are written (a grid-wide
+//     count), CTA c sums the k rows of each token for the 8-row output slabs
+//     c, c + grid, ... in slot order, with ONE bf16 rounding.
+// Every wait is bounded: a timeout sets a sticky status bit, records where,
+// and the thread carries on (the call's result is then undefined).
+#pragma once
+
+#include "kernels.cuh"
+#include "routing.cuh"
+
+namespace wse {
+
+namespace layer_detail {
+
+// shared-memory map (bytes)
+constexpr uint32_t kOffFull = 0;     // [8] gate/up stage: data landed (1 arrival + tx)
+constexpr uint32_t kOffEmpty = 64;   // [8] gate/up stage: read by the 8 consumer warps
+constexpr uint32_t kOffReady = 128;  // [8] gate/up stage: tile id written (1 arrival)
+constexpr uint32_t kOffRedBar = 192; // [8] reduction slot: 8 partials written
+constexpr uint32_t kOffDone = 256;   // [1] all consumer warps left the gate/up loop
+constexpr uint32_t kOffStatic = 520; // [1] all consumer warps reduced the static gate/up tiles
+constexpr uint32_t kOffLevel1 = 528;  // [1] every CTA's static gate/up tiles reduced (publisher)
+constexpr uint32_t kOffLevel2 = 536;  // [1] every CTA's gate/up tiles reduced (publisher)
+constexpr uint32_t kOffCall = 544;    // u64: the call's index on the grid counters (1, 2, ...)
+constexpr uint32_t kOffDFull = 264;  // [8] down stage: data landed (1 arrival + tx)
+constexpr uint32_t kOffDEmpty = 328; // [8] down stage: read by the 8 consumer warps
+constexpr uint32_t kOffDReady = 392; // [8] down stage: super-tile id written (1 arrival)
+constexpr uint32_t kOffTile = 456;   // [8] int: tile id in each gate/up stage (-1: no more)
+constexpr uint32_t kOffDTile = 488;  // [8] int: super-tile id in each down stage (-1: no more)
+constexpr uint32_t kRingOff = 1024;
+constexpr int kRedSlots = 8;
+constexpr uint32_t kRedBytes = kRedSlots * kConsumerWarps * 32 * 16;
+constexpr int kStaticNum = 3, kStaticDen = 4;  // statically split share of the groups
+static_assert(kMaxDownStages <= 8 && kMaxGateUpStages <= 8, "barrier map");
+static_assert(kOffDTile + 4 * kMaxDownStages <= kOffStatic && kOffCall + 8 <= kRingOff, "map");
+static_assert(kMaxGateUpStages < kRedSlots, "reduction slots must outnumber ring stages");
+
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Count this CTA in at a grid-wide counter: release fence, then an atomic
+// add whose result nobody waits for.
+__device__ __forceinline__ void grid_count(unsigned* word) {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(word) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void stamp(const LayerArgs& a, int slot) {
+  if (a.trace) a.ws.trace[(size_t)blockIdx.x * kTraceSlots + slot] = global_timer_ns();
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide arrival, called by ONE thread per CTA right after the threads
+// whose writes it publishes have synchronised with it (a CTA barrier or an
+// mbarrier): its fence makes those writes visible device-wide before it
+// arrives (one fence per CTA -- under full HBM load a fence from every
+// thread stalls the SM).  The 64-bit count is never reset: every use adds
+// exactly gridDim.x per call, so an arrival that returned `old` is complete
+// when the count reaches the next multiple of gridDim.x above it.  Returns
+// that target.
+__device__ __forceinline__ unsigned long long grid_arrive(unsigned* word) {
+  // release pattern: an acq_rel fence then the (relaxed) arrival; a
+  // sequentially consistent fence is not needed and costs far more while
+  // bulk copies are in flight
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  const unsigned long long G = gridDim.x;
+  const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(word), 1ull);
+  return (old / G + 1ull) * G;
+}
+
+// Bounded acquire-spin until the count at `word` reaches `target`.
+__device__ inline bool grid_wait(const Workspace& ws, const unsigned* word, unsigned long long target,
+                                 int phase) {
+  const unsigned long long* cnt = reinterpret_cast<const unsigned long long*>(word);
+  if (ld_acquire64(cnt) >= target) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(32);
+    if (ld_acquire64(cnt) >= target) return true;
+    const unsigned long long dt = global_timer_ns() - t0;
+    if (dt > kWaitTimeoutNs) {
+      record_timeout(ws, phase, kErrTimeoutGrid, (int)(target % gridDim.x), 0, 0, dt);
+      return false;
+    }
+  }
+}
+
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+}  // namespace layer_detail
+
+template <int KPW>  // H / 256: 32-wide k chunks per warp in the gate/up GEMV
+__global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs a) {
+  using namespace layer_detail;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) stamp(a, 19);  // CTA started
+  const int S = a.gu_stages, SD = a.d_stages;
+  const int NP = a.M * a.K;
+  const uint32_t sb = smem_u32(smem);
+  int* stage_tile = reinterpret_cast<int*>(smem + kOffTile);
+  int* dstage_tile = reinterpret_cast<int*>(smem + kOffDTile);
+  const uint32_t dsuper = kConsumerWarps * a.d_tile;  // bytes of a down stage
+  uint8_t* ring = smem + kRingOff;
+  const uint32_t ring_u32 = sb + kRingOff;
+  float4* red = reinterpret_cast<float4*>(ring + (size_t)S * a.gu_tile);
+  const SmemRouting rt = routing_carve(ring + a.ring_bytes, NP, a.E);
+  auto full = [&](int s) { return sb + kOffFull + 8u * s; };
+  auto empty = [&](int s) { return sb + kOffEmpty + 8u * s; };
+  auto ready = [&](int s) { return sb + kOffReady + 8u * s; };
+  auto redbar = [&](int r) { return sb + kOffRedBar + 8u * r; };
+  auto dfull = [&](int d) { return sb + kOffDFull + 8u * d; };
+  auto dempty = [&](int d) { return sb + kOffDEmpty + 8u * d; };
+  auto dready = [&](int d) { return sb + kOffDReady + 8u * d; };
+  const uint32_t done = sb + kOffDone;
+  const uint32_t static_bar = sb + kOffStatic;
+  const uint32_t level1 = sb + kOffLevel1, level2 = sb + kOffLevel2;
+  unsigned long long* call_idx = reinterpret_cast<unsigned long long*>(smem + kOffCall);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kConsumerWarps);
+      mbar_init(ready(s), 1);
+    }
+    for (int r = 0; r < kRedSlots; ++r) mbar_init(redbar(r), kConsumerWarps);
+    mbar_init(done, kConsumerWarps);
+    mbar_init(static_bar, kConsumerWarps);
+    mbar_init(level1, 1);
+    mbar_init(level2, 1);
+    for (int d = 0; d < SD; ++d) {
+      mbar_init(dfull(d), 1);
+      mbar_init(dempty(d), kConsumerWarps);
+      mbar_init(dready(d), 1);
+    }
+    fence_mbar_init();
+  }
+  for (int e = tid; e < a.E; e += kExpertThreads) rt.mask[e] = 0ull;
+  for (int p = tid; p < NP; p += kExpertThreads) rt.pair_list[p] = 0;
+  if (tid < 2) rt.scal[tid] = 0;
+
+  // ---- 1. producer-independent: this CTA's slice of the router weight
+  const int units = ((a.E + 7) / 8) * a.ks;
+  const int gw = warp < kConsumerWarps ? warp : 0;
+  GemvUnit gu = gemv_unit(blockIdx.x, a.ks, a.H, gw);
+  uint4 wb[KPW];
+  if ((int)blockIdx.x < units && warp < kConsumerWarps) gemv_load_w<KPW>(a.w_router, a.E, a.H, gu, lane, wb);
+
+  if (tid == 0) stamp(a, 20);  // prologue done
+  pdl_wait();               // x and the workspace belong to this call now
+  pdl_launch_dependents();  // the next call's prologue may start as SMs free up
+  if (tid == 0) stamp(a, 0);
+
+  // ---- 2. router matvec, then every partial logit is published
+  const size_t plane = (size_t)kMaxTokens * a.E;
+  for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    if (unit != (int)blockIdx.x) {
+      gu = gemv_unit(unit, a.ks, a.H, gw);
+      if (warp < kConsumerWarps) gemv_load_w<KPW>(a.w_router, a.E, a.H, gu, lane, wb);
+    }
+    for (int mb = 0; mb * 16 < a.M; ++mb) {
+      if (warp < kConsumerWarps) red[warp * 32 + lane] = gemv_tokens<KPW>(a.x, a.M, a.H, gu, mb, lane, wb);
+      __syncthreads();
+      if (warp == 0) gemv_store(red, gu, mb, a.M, a.E, plane, a.ws.part, lane);
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    stamp(a, 1);
+    if (blockIdx.x == 0) {  // the per-call work counters; nothing reads them before the barrier
+      a.ws.sync[kSyncGateUpNext] = 0u;
+      a.ws.sync[kSyncDownNext] = 0u;
+    }
+    const unsigned long long t1 = grid_arrive(a.ws.sync + kSyncCount);
+    grid_wait(a.ws, a.ws.sync + kSyncCount, t1, 1);
+    *call_idx = (t1 / gridDim.x + 1ull) / 2ull;  // two barrier arrivals per CTA per call
+    stamp(a, 2);
+  }
+  __syncthreads();
+
+  // ---- 3. top-k of every token, compaction (every CTA, shared memory only)
+  for (int m = warp; m < a.M; m += kExpertThreads / 32) {
+    const float w = topk_dispatch(a.ws.part + (size_t)m * a.E, plane, a.ks, a.bias, a.E, a.K, lane,
+                                  a.ws.status, rt.s_e + m * a.K);
+    __syncwarp();
+    if (lane < a.K) {
+      const int p = m * a.K + lane;
+      const int idx = rt.s_e[p];
+      rt.s_w[p] = w;
+      atomicOr(&rt.mask[idx], 1ull << m);
+      if (blockIdx.x == 0) {
+        a.topk_idx[p] = idx;
+        if (a.topk_w) a.topk_w[p] = w;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) stamp(a, 12);
+  compact_masks(rt, a.M, a.K, a.E);
+  const int n_groups = rt.scal[0];
+  if (tid == 0) stamp(a, 13);
+  if (blockIdx.x == 0) {  // a copy for inspection (moe_read_routing); nothing reads it back
+    for (int i = tid; i < NP; i += kExpertThreads) {
+      a.ws.pair_list[i] = rt.pair_list[i];
+      a.ws.pair_w[i] = rt.s_w[i];
+      if (i < n_groups) {
+        a.ws.grp_expert[i] = rt.grp_expert[i];
+        a.ws.grp_start[i] = rt.grp_start[i];
+        a.ws.grp_cnt[i] = rt.grp_cnt[i];
+      }
+    }
+    if (tid == 0) {
+      *a.ws.n_groups = n_groups;
+      *a.ws.n_active = rt.scal[1];
+    }
+  }
+  if (tid == 0) stamp(a, 3);
+
+  const int TPG = 2 * a.I / kGateUpTileRows;  // gate/up tiles per group
+  const int T_gu = n_groups * TPG;
+  const int SL = a.H / kDownTileRows;         // 8-row output slabs per group
+  const int SPG = SL / kConsumerWarps;        // down super tiles per group
+  const int T_d = n_groups * SPG;
+  // groups [0, g_static) are split statically in both GEMVs: their gate/up
+  // tiles are all in the static share, and so are their down tiles
+  const int g_static = n_groups * kStaticNum / kStaticDen;
+
+  if (warp == kPublisherWarp) {
+    // =============================================================== publisher
+    if (lane != 0) return;
+    unsigned long long waited = 0;
+    const unsigned long long target = *call_idx * gridDim.x;
+    // static gate/up tiles reduced here -> counted; every CTA counted -> level 1
+    if (!mbar_wait(static_bar, 0, &waited)) {
+      record_timeout(a.ws, 2, kErrTimeoutReduce, -3, 0, static_bar, waited);
+      return;
+    }
+    grid_count(a.ws.sync + kSyncStaticDone);
+    stamp(a, 18);
+    if (!grid_wait(a.ws, a.ws.sync + kSyncStaticDone, target, 2)) return;
+    mbar_arrive(level1);
+    stamp(a, 6);
+    // all gate/up tiles reduced here -> counted; every CTA counted -> level 2
+    if (!mbar_wait(done, 0, &waited)) {
+      record_timeout(a.ws, 2, kErrTimeoutReduce, -4, 0, done, waited);
+      return;
+    }
+    grid_count(a.ws.sync + kSyncGateUpDone);
+    if (!grid_wait(a.ws, a.ws.sync + kSyncGateUpDone, target, 2)) return;
+    mbar_arrive(level2);
+    stamp(a, 17);
+    return;
+  }
+
+  if (warp == kProducerWarp) {
+    // ================================================================ producer
+    if (lane != 0) return;
+    unsigned long long waited = 0;
+    // static share of each phase, then single tiles from the shared tail
+    const int Ts = g_static * TPG;
+    const int s0 = (int)((long long)Ts * blockIdx.x / gridDim.x);
+    const int s1 = (int)((long long)Ts * (blockIdx.x + 1) / gridDim.x);
+    const int Ts2 = g_static * SPG;
+    const int q0 = (int)((long long)Ts2 * blockIdx.x / gridDim.x);
+    const int q1 = (int)((long long)Ts2 * (blockIdx.x + 1) / gridDim.x);
+    unsigned* next_gu = a.ws.sync + kSyncGateUpNext;
+    unsigned* next_d = a.ws.sync + kSyncDownNext;
+    // one tile of each shared tail, taken early so the round trip is hidden
+    int dyn_gu = Ts + (int)atomicAdd(next_gu, 1u);
+    int dyn_d = Ts2 + (int)atomicAdd(next_d, 1u);
+    bool ok = true;
+    int level = 0;  // readiness of the h rows seen so far (see the publisher)
+    // ---- gate/up tiles
+    int j = 0;
+    for (;; ++j) {
+      int tile;
+      if (s0 + j < s1) {
+        tile = s0 + j;
+      } else {
+        tile = dyn_gu;
+        if (tile < T_gu) dyn_gu = Ts + (int)atomicAdd(next_gu, 1u);
+      }
+      if (tile >= T_gu) break;
+      const int s = j % S;
+      if (j >= S && !mbar_wait(empty(s), ((j / S) - 1) & 1, &waited)) {
+        record_timeout(a.ws, 2, kErrTimeoutEmpty, j, S, empty(s), waited);
+        ok = false;
+        break;
+      }
+      stage_tile[s] = tile;
+      mbar_arrive(ready(s));
+      const int g = tile / TPG, tt = tile - g * TPG;
+      mbar_arrive_expect_tx(full(s), a.gu_tile);
+      bulk_g2s_chunked(ring_u32 + (uint32_t)s * a.gu_tile,
+                       a.w_gate_up + ((size_t)rt.grp_expert[g] * TPG + tt) * a.gu_tile, a.gu_tile, full(s));
+    }
+    const int n_gu = j;
+    if (ok) {  // end marker for the consumers
+      const int s = j % S;
+      if (j >= S && !mbar_wait(empty(s), ((j / S) - 1) & 1, &waited)) {
+        record_timeout(a.ws, 2, kErrTimeoutEmpty, j, S, empty(s), waited);
+        ok = false;
+      } else {
+        stage_tile[s] = -1;
+        mbar_arrive(ready(s));
+      }
+    }
+    stamp(a, 9);
+    if (a.trace) a.ws.trace[(size_t)blockIdx.x * kTraceSlots + 11] = (unsigned long long)n_gu;
+    // the readiness level the h rows of down group g need
+    auto ensure_ready = [&](int g) -> bool {
+      const int need = g < g_static ? 1 : 2;
+      if (level >= need) return true;
+      if (!mbar_wait(need == 1 ? level1 : level2, 0, &waited)) {
+        record_timeout(a.ws, 3, kErrTimeoutReduce, -5 - need, SD, need == 1 ? level1 : level2, waited);
+        return false;
+      }
+      level = need;
+      return true;
+    };
+    // ---- down super tiles.  The first use of a down stage waits until the
+    // ring bytes under it are free: the gate/up stages there consumed for
+    // the last time (taken in consumption order), and for bytes over the
+    // reduction area, every consumer warp out of the gate/up loop.
+    uint32_t released = 0u;
+    for (int s = 0; s < S; ++s)
+      if (s >= n_gu) released |= 1u << s;
+    int r = 0;
+    bool done_seen = false;
+    auto release_until = [&](uint32_t need) -> bool {
+      while ((released & need) != need) {
+        if (r < S) {
+          const int jf = n_gu - S + r++;
+          if (jf < 0) continue;
+          const int s = jf % S;
+          if (!mbar_wait(empty(s), (jf / S) & 1, &waited)) {
+            record_timeout(a.ws, 3, kErrTimeoutEmpty, jf, S, empty(s), waited);
+            return false;
+          }
+          released |= 1u << s;
+        } else if (!done_seen) {
+          if (!mbar_wait(done, 0, &waited)) {
+            record_timeout(a.ws, 3, kErrTimeoutEmpty, -1, S, done, waited);
+            return false;
+          }
+          fence_proxy_async_smem();  // the reduction area was last written with ordinary stores
+          released = 0xffffffffu;
+          done_seen = true;
+        } else {
+          return false;
+        }
+      }
+      return true;
+    };
+    int j2 = 0;
+    for (; ok; ++j2) {
+      int tile;
+      if (q0 + j2 < q1) {
+        tile = q0 + j2;
+      } else {
+        tile = dyn_d;
+        if (tile < T_d) dyn_d = Ts2 + (int)atomicAdd(next_d, 1u);
+      }
+      if (tile >= T_d) break;
+      const int s = j2 % SD;
+      if (j2 < SD) {
+        if (!release_until(a.d_need[s])) {
+          ok = false;
+          break;
+        }
+      } else if (!mbar_wait(dempty(s), ((j2 / SD) - 1) & 1, &waited)) {
+        record_timeout(a.ws, 3, kErrTimeoutEmpty, j2, SD, dempty(s), waited);
+        ok = false;
+        break;
+      }
+      // the copy first (weights never depend on h), then the id once the
+      // group's h rows are ready
+      const int g = tile / SPG, q = tile - g * SPG;
+      mbar_arrive_expect_tx(dfull(s), dsuper);
+      bulk_g2s_chunked(ring_u32 + (uint32_t)s * dsuper,
+                       a.w_down + ((size_t)rt.grp_expert[g] * SL + (size_t)q * kConsumerWarps) * a.d_tile,
+                       dsuper, dfull(s));
+      if (!ensure_ready(g)) {
+        ok = false;
+        break;
+      }
+      dstage_tile[s] = tile;
+      mbar_arrive(dready(s));
+    }
+    if (a.trace) a.ws.trace[(size_t)blockIdx.x * kTraceSlots + 16] = (unsigned long long)j2;
+    if (ok) {  // end marker (a first use needs no free bytes: only the id is written)
+      const int s = j2 % SD;
+      if (j2 >= SD && !mbar_wait(dempty(s), ((j2 / SD) - 1) & 1, &waited)) {
+        record_timeout(a.ws, 3, kErrTimeoutEmpty, j2, SD, dempty(s), waited);
+      } else {
+        dstage_tile[s] = -1;
+        mbar_arrive(dready(s));
+      }
+    }
+    stamp(a, 10);
+    return;
+  }
+
+  // ================================================================ consumers
+  const int g4 = lane >> 2, t4 = lane & 3;
+  unsigned long long waited = 0;
+  {
+    // ---- 4. gate/up + SwiGLU
+    uint4 xa[KPW], xb[KPW];  // token rows g4 and g4 + 8 of the group: this warp's k chunks
+    int cur_g = -1, start = 0, cnt = 0;
+    // this CTA's statically split tiles come first: after the last of them
+    // (or at once if it has none) the warp reports them reduced
+    const int Ts = g_static * TPG;
+    const int n_static = (int)((long long)Ts * (blockIdx.x + 1) / gridDim.x) -
+                         (int)((long long)Ts * blockIdx.x / gridDim.x);
+    if (n_static == 0 && lane == 0) mbar_arrive(static_bar);
+    for (int j = 0;; ++j) {
+      const int s = j % S;
+      const uint32_t ph = (uint32_t)(j / S) & 1u;
+      if (!warp_wait(ready(s), ph, &waited)) {
+        record_timeout(a.ws, 2, kErrTimeoutFull, j, S, ready(s), waited);
+        break;
+      }
+      const int tile = stage_tile[s];
+      if (tile < 0) break;
+      const int g = tile / TPG, tt = tile - g * TPG;
+      if (g != cur_g) {
+        // rows beyond the group's count repeat its first token, never stored
+        start = rt.grp_start[g];
+        cnt = rt.grp_cnt[g];
+        const int tok0 = rt.pair_list[start + (g4 < cnt ? g4 : 0)] / a.K;
+        const int tok1 = rt.pair_list[start + (g4 + 8 < cnt ? g4 + 8 : 0)] / a.K;
+        const uint4* x0 = reinterpret_cast<const uint4*>(a.x + (size_t)tok0 * a.H) + t4;
+        const uint4* x1 = reinterpret_cast<const uint4*>(a.x + (size_t)tok1 * a.H) + t4;
+#pragma unroll
+        for (int q = 0; q < KPW; ++q) {
+          xa[q] = x0[4 * (warp * KPW + q)];
+          xb[q] = x1[4 * (warp * KPW + q)];
+        }
+        cur_g = g;
+      }
+      if (!warp_wait(full(s), ph, &waited)) {
+        record_timeout(a.ws, 2, kErrTimeoutFull, j, S, full(s), waited);
+        break;
+      }
+      if (j == 0 && tid == 0) stamp(a, 4);
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4* wp = reinterpret_cast<const uint4*>(ring + (size_t)s * a.gu_tile) + (warp * KPW) * 32 + lane;
+#pragma unroll
+      for (int q = 0; q < KPW; ++q) {
+        const uint4 b = wp[q * 32];
+        mma_bf16(c0, xa[q].x, xb[q].x, xa[q].y, xb[q].y, b.x, b.y);
+        mma_bf16(c1, xa[q].z, xb[q].z, xa[q].w, xb[q].w, b.z, b.w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(s));  // stage free for the producer
+
+      const int slot = j & (kRedSlots - 1);
+      red[(slot * kConsumerWarps + warp) * 32 + lane] =
+          make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(redbar(slot));
+      if (warp == slot) {  // this tile's reducer (rotates over the warps)
+        if (!warp_wait(redbar(slot), (uint32_t)(j >> 3) & 1u, &waited)) {
+          record_timeout(a.ws, 2, kErrTimeoutReduce, j, S, redbar(slot), waited);
+          break;
+        }
+        float4 acc = red[(slot * kConsumerWarps) * 32 + lane];
+#pragma unroll
+        for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
+          const float4 v = red[(slot * kConsumerWarps + w2) * 32 + lane];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        // (acc.x, acc.y) = (gate, up) of group token g4, intermediate row
+        // 4 tt + t4; (acc.z, acc.w) the same for group token g4 + 8
+        const int r = 4 * tt + t4;
+        if (g4 < cnt) a.ws.h[(size_t)(start + g4) * a.I + r] = __float2bfloat16_rn(silu(acc.x) * acc.y);
+        if (g4 + 8 < cnt)
+          a.ws.h[(size_t)(start + g4 + 8) * a.I + r] = __float2bfloat16_rn(silu(acc.z) * acc.w);
+      }
+      if (j == n_static - 1) {  // every static tile of this warp's share is reduced
+        __syncwarp();
+        if (lane == 0) mbar_arrive(static_bar);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done);
+    if (tid == 0) stamp(a, 5);
+  }
+
+  // (this CTA's h rows are all written: the `done` barrier tells the
+  // publisher, and the producer holds back each down tile until its group
+  // is ready -- the consumers go straight on)
+
+  {
+    // ---- 5. down GEMV, weighted rows y[pair] = w_pair * (W_d h_pair);
+    // warp w takes slab w of every super tile
+    const int kpd = a.I / 32;  // 32-wide k chunks of a down row (<= kMaxDownChunks)
+    uint4 ha[kMaxDownChunks], hb[kMaxDownChunks];
+    int pid0 = -1, pid1 = -1;
+    float pw0 = 0.f, pw1 = 0.f;
+    int cur_g = -1;
+    for (int j = 0;; ++j) {
+      const int s = j % SD;
+      const uint32_t ph = (uint32_t)(j / SD) & 1u;
+      if (!warp_wait(dready(s), ph, &waited)) {
+        record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dready(s), waited);
+        break;
+      }
+      const int tile = dstage_tile[s];
+      if (tile < 0) break;
+      const int g = tile / SPG;
+      const int sl = (tile - g * SPG) * kConsumerWarps + warp;
+      if (g != cur_g) {
+        const int start = rt.grp_start[g], cnt = rt.grp_cnt[g];
+        const uint4* h0 =
+            reinterpret_cast<const uint4*>(a.ws.h + (size_t)(start + (g4 < cnt ? g4 : 0)) * a.I) + t4;
+        const uint4* h1 =
+            reinterpret_cast<const uint4*>(a.ws.h + (size_t)(start + (g4 + 8 < cnt ? g4 + 8 : 0)) * a.I) + t4;
+#pragma unroll
+        for (int q = 0; q < kMaxDownChunks; ++q) {
+          if (q < kpd) {
+            ha[q] = __ldcg(h0 + 4 * q);  // written by other SMs in this grid: L2, not L1
+            hb[q] = __ldcg(h1 + 4 * q);
+          }
+        }
+        pid0 = g4 < cnt ? rt.pair_list[start + g4] : -1;
+        pid1 = g4 + 8 < cnt ? rt.pair_list[start + g4 + 8] : -1;
+        pw0 = pid0 >= 0 ? rt.s_w[pid0] : 0.f;
+        pw1 = pid1 >= 0 ? rt.s_w[pid1] : 0.f;
+        cur_g = g;
+      }
+      if (!warp_wait(dfull(s), ph, &waited)) {
+        record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dfull(s), waited);
+        break;
+      }
+      if (j == 0 && tid == 0) stamp(a, 14);
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4* bp = reinterpret_cast<const uint4*>(ring + (size_t)s * dsuper + (size_t)warp * a.d_tile) + lane;
+#pragma unroll
+      for (int q = 0; q < kMaxDownChunks; ++q) {
+        if (q < kpd) {
+          const uint4 b = bp[q * 32];
+          mma_bf16(c0, ha[q].x, hb[q].x, ha[q].y, hb[q].y, b.x, b.y);
+          mma_bf16(c1, ha[q].z, hb[q].z, ha[q].w, hb[q].w, b.z, b.w);
+        }
+      }
+      __syncwarp();  // every lane has read the stage
+      if (lane == 0) mbar_arrive(dempty(s));
+      // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of the slab)
+      const int row = sl * kDownTileRows + 2 * t4;
+      if (pid0 >= 0)
+        *reinterpret_cast<float2*>(a.ws.y + (size_t)pid0 * a.H + row) =
+            make_float2(pw0 * (c0[0] + c1[0]), pw0 * (c0[1] + c1[1]));
+      if (pid1 >= 0)
+        *reinterpret_cast<float2*>(a.ws.y + (size_t)pid1 * a.H + row) =
+            make_float2(pw1 * (c0[2] + c1[2]), pw1 * (c0[3] + c1[3]));
+    }
+    if (tid == 0) stamp(a, 7);
+  }
+
+  // ---- 6. every CTA's weighted rows written -> combine.  CTA c owns the
+  // 8-row output slabs c, c + grid, ...: each token's k rows summed in slot
+  // order, ONE bf16 rounding.
+  consumers_sync();
+  if (tid == 0) {
+    grid_count(a.ws.sync + kSyncCount);
+    grid_wait(a.ws, a.ws.sync + kSyncCount, 2ull * *call_idx * gridDim.x, 3);
+  }
+  consumers_sync();
+  if (tid == 0) stamp(a, 15);
+  const int nthr = kConsumerWarps * 32;
+  const int n_own = SL > (int)blockIdx.x ? (SL - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int per = a.M * kDownTileRows;
+  for (int it = tid; it < n_own * per; it += nthr) {
+    const int sl = (int)blockIdx.x + (it / per) * (int)gridDim.x;
+    const int m = (it % per) / kDownTileRows;
+    const int r = sl * kDownTileRows + (it % kDownTileRows);
+    const float* yr = a.ws.y + (size_t)m * a.K * a.H + r;
+    float sum = 0.f;
+    for (int k0 = 0; k0 < a.K; k0 += 8) {  // 8 loads in flight, summed in slot order
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = k0 + i < a.K ? __ldcg(yr + (size_t)(k0 + i) * a.H) : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < a.K) sum += v[i];
+    }
+    a.out[(size_t)m * a.H + r] = __float2bfloat16_rn(sum);
+  }
+  if (tid == 0) stamp(a, 8);
+}
+
+}  // namespace wse

@@ -1,6 +1,7 @@
 // moe_api.cu -- host runtime behind include/moe.h: argument checks, weight
-// re-layout at create, workspace, the three PDL-chained launches, and the
-// per-(handle, M) CUDA graph cache.
+// re-layout at create, workspace, the layer kernel's launch (PDL-chained to
+// the previous work on the stream), and the per-(handle, M) CUDA graph
+// cache.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -13,6 +14,7 @@
 
 #include "kernels.cuh"
 #include "moe.h"
+#include "routing.cuh"
 
 using namespace wse;
 
@@ -73,12 +75,12 @@ struct moe_layer {
   void* ws_mem = nullptr;
   size_t ws_bytes = 0, weight_bytes = 0;
   Workspace ws{};
-  int s2 = 0, s3 = 0;
-  uint32_t tile2 = 0, tile3 = 0;
-  size_t smem1 = 0, smem2 = 0, smem3 = 0;  // largest dynamic shared memory per kernel
-  RouterKernel k1 = nullptr;
-  GateUpKernel k2 = nullptr;
-  DownKernel k3 = nullptr;
+  int ks = 1;               // hidden-dim split of the router matvec
+  int s_gu = 0, s_d = 0;    // gate/up ring depth, down stages
+  uint32_t tile_gu = 0, tile_d = 0, ring_bytes = 0;
+  uint32_t d_need[kMaxDownStages] = {};  // gate/up stages (bit 31: reduction area) under each down stage
+  size_t smem_max = 0;      // dynamic shared memory at M = MOE_MAX_TOKENS
+  LayerKernel kernel = nullptr;
   std::map<int, GraphEntry> graphs;
   cudaStream_t cap_stream = nullptr;
 };
@@ -110,36 +112,29 @@ int cuda_fail(cudaError_t e, const char* what) {
   return MOE_ERR_CUDA;
 }
 
-// Enqueue the three kernels.  ev (4 events) brackets them for profiling; the
+// Enqueue the layer kernel.  ev (2 events) brackets it for profiling; the
 // records are external event nodes when the stream is being captured.
-int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, int M,
-               cudaStream_t st, bool pdl, cudaEvent_t* ev) {
-  RouterArgs ra{};
-  ra.x = static_cast<const __nv_bfloat16*>(x);
-  ra.w_router = h->w_router;
-  ra.bias = h->bias;
-  ra.M = M; ra.H = h->H; ra.E = h->E; ra.K = h->K;
-  ra.topk_idx = idx;
-  ra.topk_w = tw;
-  ra.ws = h->ws;
-
-  GateUpArgs ga{};
-  ga.w_gate_up = h->w_gu;
-  ga.x = ra.x;
-  ga.topk_idx = idx;
-  ga.M = M; ga.H = h->H; ga.I = h->I; ga.K = h->K; ga.E = h->E;
-  ga.stages = h->s2;
-  ga.tile_bytes = h->tile2;
-  ga.ws = h->ws;
-
-  DownArgs da{};
-  da.w_down = h->w_d;
-  da.out = static_cast<__nv_bfloat16*>(out);
-  da.topk_idx = idx;
-  da.M = M; da.H = h->H; da.I = h->I; da.K = h->K; da.E = h->E;
-  da.stages = h->s3;
-  da.tile_bytes = h->tile3;
-  da.ws = h->ws;
+int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, int M,
+                 cudaStream_t st, bool pdl, bool trace, cudaEvent_t* ev) {
+  LayerArgs la{};
+  la.x = static_cast<const __nv_bfloat16*>(x);
+  la.w_router = h->w_router;
+  la.bias = h->bias;
+  la.w_gate_up = h->w_gu;
+  la.w_down = h->w_d;
+  la.out = static_cast<__nv_bfloat16*>(out);
+  la.topk_idx = idx;
+  la.topk_w = tw;
+  la.M = M; la.H = h->H; la.E = h->E; la.K = h->K; la.I = h->I;
+  la.ks = h->ks;
+  la.gu_stages = h->s_gu;
+  la.d_stages = h->s_d;
+  la.gu_tile = h->tile_gu;
+  la.d_tile = h->tile_d;
+  la.ring_bytes = h->ring_bytes;
+  la.trace = trace ? 1 : 0;
+  for (int d = 0; d < kMaxDownStages; ++d) la.d_need[d] = h->d_need[d];
+  la.ws = h->ws;
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -148,9 +143,11 @@ int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, 
   c.stream = st;
   c.attrs = pdl ? attr : nullptr;
   c.numAttrs = pdl ? 1 : 0;
+  c.gridDim = dim3(h->n_sms);
+  c.blockDim = dim3(kExpertThreads);
+  c.dynamicSmemBytes = layer_smem_bytes(h->ring_bytes, M * h->K, h->E);
 
   cudaError_t e;
-  // under stream capture the records must be external event nodes
   unsigned ev_flags = cudaEventRecordDefault;
   if (ev) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -158,21 +155,8 @@ int launch_all(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, 
     if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
   }
   if (ev && (e = cudaEventRecordWithFlags(ev[0], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
-  c.gridDim = dim3((h->E + kRouterExpertsPerCta - 1) / kRouterExpertsPerCta);
-  c.blockDim = dim3(kRouterThreads);
-  c.dynamicSmemBytes = router_smem_bytes(M, h->H, h->K, h->E);
-  if ((e = cudaLaunchKernelEx(&c, h->k1, ra)) != cudaSuccess)
-    return cuda_fail(e, "router launch");
+  if ((e = cudaLaunchKernelEx(&c, h->kernel, la)) != cudaSuccess) return cuda_fail(e, "layer kernel launch");
   if (ev && (e = cudaEventRecordWithFlags(ev[1], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
-  c.gridDim = dim3(h->n_sms);
-  c.blockDim = dim3(kExpertThreads);
-  c.dynamicSmemBytes = gateup_smem_bytes(h->s2, h->tile2, M * h->K, h->E);
-  if ((e = cudaLaunchKernelEx(&c, h->k2, ga)) != cudaSuccess) return cuda_fail(e, "gate/up launch");
-  if (ev && (e = cudaEventRecordWithFlags(ev[2], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
-  c.blockDim = dim3(kDownThreadsPerCta);
-  c.dynamicSmemBytes = down_smem_bytes(h->s3, h->tile3, M * h->K, h->E, h->H);
-  if ((e = cudaLaunchKernelEx(&c, h->k3, da)) != cudaSuccess) return cuda_fail(e, "down launch");
-  if (ev && (e = cudaEventRecordWithFlags(ev[3], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
   return MOE_OK;
 }
 
@@ -202,12 +186,12 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
                         const void* w_gate_up, const void* w_down) {
   g_last_error.clear();
   // ---- argument checks (no CUDA call before these pass) ----
-  if (hidden <= 0 || hidden % 256 != 0 || !gateup_kernel_for(hidden / 256)) {
+  if (hidden <= 0 || hidden % 256 != 0 || !layer_kernel_for(hidden / 256)) {
     set_err("hidden = %d unsupported: need a multiple of 256 with hidden/256 in {1,2,4,5,8,10,12,16}",
             hidden);
     return nullptr;
   }
-  if (inter <= 0 || inter % 16 != 0 || !down_kernel_for(inter / 16)) {
+  if (inter != 128 && inter != 256 && inter != 512) {
     set_err("inter = %d unsupported: need one of {128, 256, 512}", inter);
     return nullptr;
   }
@@ -217,6 +201,10 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
     return nullptr;
   }
   if (!w_router || !w_gate_up || !w_down) { set_err("null weight pointer"); return nullptr; }
+  if (!aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down)) {
+    set_err("weight pointers must be 16-byte aligned");
+    return nullptr;
+  }
 
   // ---- device ----
   int dev = 0;
@@ -229,7 +217,7 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
     return nullptr;
   }
   cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, router_kernel_for(hidden / 256))) != cudaSuccess) {
+  if ((e = cudaFuncGetAttributes(&fa, layer_kernel_for(hidden / 256))) != cudaSuccess) {
     cuda_fail(e, "kernel image");
     return nullptr;
   }
@@ -238,32 +226,40 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   h->H = hidden; h->E = n_experts; h->K = topk; h->I = inter;
   h->dev = dev;
   h->n_sms = prop.multiProcessorCount;
-  h->k1 = router_kernel_for(hidden / 256);
-  h->k2 = gateup_kernel_for(hidden / 256);
-  h->k3 = down_kernel_for(inter / 16);
-  h->tile2 = (uint32_t)(kGateUpTileRows * hidden * 2);
-  h->tile3 = (uint32_t)(kDownTileRows * inter * 2);
+  h->kernel = layer_kernel_for(hidden / 256);
+  h->tile_gu = (uint32_t)(kGateUpTileRows * hidden * 2);
+  h->tile_d = (uint32_t)(kDownTileRows * inter * 2);
+  h->ks = gemv_split(hidden, n_experts, h->n_sms);
 
-  // Ring depths, sized for the largest call (M = MOE_MAX_TOKENS): both expert
-  // kernels take what the opt-in shared memory allows (one CTA per SM; deep
-  // rings keep enough bytes in flight to cover the loaded HBM latency).
+  // Ring sized for the largest call (M = MOE_MAX_TOKENS): the gate/up stages
+  // plus the reduction area behind them, and the down stages over the same
+  // bytes, take what the opt-in shared memory leaves after the routing area
+  // (one CTA per SM; deep rings keep enough bytes in flight to cover the
+  // loaded HBM latency).
   const size_t optin = prop.sharedMemPerBlockOptin;
   const int np_max = kMaxTokens * topk;
-  const size_t gu_fixed = gateup_smem_bytes(0, h->tile2, np_max, n_experts);
-  const size_t dn_fixed = down_smem_bytes(0, h->tile3, np_max, n_experts, hidden);
-  h->s2 = optin > gu_fixed ? (int)std::min<size_t>(kMaxGateUpStages, (optin - gu_fixed) / h->tile2) : 0;
-  const size_t down_budget = optin;
-  // down-kernel stages come in whole sets of one per consumer warp
-  h->s3 = down_budget > dn_fixed ? (int)std::min<size_t>(kMaxDownStages, (down_budget - dn_fixed) / h->tile3) : 0;
-  h->s3 -= h->s3 % kConsumerWarps;
-  if (h->s2 < 2 || h->s3 < kConsumerWarps) {
+  const size_t fixed = layer_smem_bytes(0, np_max, n_experts);
+  const size_t avail = optin > fixed ? optin - fixed : 0;
+  const size_t red = layer_reduction_bytes();
+  h->s_gu = avail > red ? (int)std::min<size_t>(kMaxGateUpStages, (avail - red) / h->tile_gu) : 0;
+  const size_t d_stage = (size_t)kConsumerWarps * h->tile_d;  // one slab per consumer warp
+  h->s_d = (int)std::min<size_t>(kMaxDownStages, avail / d_stage);
+  if (h->s_gu < 2 || h->s_d < 2) {
     set_err("not enough shared memory for the staging rings");
     free_layer(h);
     return nullptr;
   }
-  h->smem1 = router_smem_bytes(kMaxTokens, hidden, topk, n_experts);
-  h->smem2 = gateup_smem_bytes(h->s2, h->tile2, np_max, n_experts);
-  h->smem3 = down_smem_bytes(h->s3, h->tile3, np_max, n_experts, hidden);
+  h->ring_bytes = (uint32_t)std::max<size_t>((size_t)h->s_gu * h->tile_gu + red, (size_t)h->s_d * d_stage);
+  // which earlier occupants of the ring bytes each down stage must wait for
+  for (int d = 0; d < h->s_d; ++d) {
+    const size_t lo = (size_t)d * d_stage, hi = lo + d_stage;
+    uint32_t need = 0;
+    for (int st = 0; st < h->s_gu; ++st)
+      if (lo < (size_t)(st + 1) * h->tile_gu && (size_t)st * h->tile_gu < hi) need |= 1u << st;
+    if (hi > (size_t)h->s_gu * h->tile_gu) need |= 1u << 31;  // reduction area (or beyond)
+    h->d_need[d] = need;
+  }
+  h->smem_max = layer_smem_bytes(h->ring_bytes, np_max, n_experts);
 
   AllocCounter ac;
   const size_t E = n_experts, H = hidden, I = inter;
@@ -282,13 +278,14 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   const size_t np = (size_t)kMaxTokens * topk;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-  const size_t o_status = take(4), o_diag = take(32), o_count = take(4), o_ng = take(4), o_na = take(4);
+  const size_t o_status = take(4), o_diag = take(32), o_sync = take(kSyncWords * 4);
+  const size_t o_part = take((size_t)h->ks * kMaxTokens * E * 4);
+  const size_t o_ng = take(4), o_na = take(4);
   const size_t o_ge = take(np * 4), o_gs = take(np * 4), o_gc = take(np * 4);
   const size_t o_pl = take(np * 4), o_pw = take(np * 4);
-  const size_t o_lg = take((size_t)kMaxTokens * E * 4);
   const size_t o_h = take(np * I * 2);
   const size_t o_y = take(np * H * 4);
-  const size_t o_sc = take((H / kDownTileRows) * 4);
+  const size_t o_tr = take((size_t)h->n_sms * kTraceSlots * 8);
   h->ws_bytes = off;
   if (ac.alloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -299,7 +296,8 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   uint8_t* base = static_cast<uint8_t*>(h->ws_mem);
   h->ws.status = reinterpret_cast<int*>(base + o_status);
   h->ws.diag = reinterpret_cast<unsigned long long*>(base + o_diag);
-  h->ws.router_count = reinterpret_cast<int*>(base + o_count);
+  h->ws.sync = reinterpret_cast<unsigned*>(base + o_sync);
+  h->ws.part = reinterpret_cast<float*>(base + o_part);
   h->ws.n_groups = reinterpret_cast<int*>(base + o_ng);
   h->ws.n_active = reinterpret_cast<int*>(base + o_na);
   h->ws.grp_expert = reinterpret_cast<int*>(base + o_ge);
@@ -307,10 +305,9 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   h->ws.grp_cnt = reinterpret_cast<int*>(base + o_gc);
   h->ws.pair_list = reinterpret_cast<int*>(base + o_pl);
   h->ws.pair_w = reinterpret_cast<float*>(base + o_pw);
-  h->ws.logits = reinterpret_cast<float*>(base + o_lg);
   h->ws.h = reinterpret_cast<__nv_bfloat16*>(base + o_h);
   h->ws.y = reinterpret_cast<float*>(base + o_y);
-  h->ws.slab_count = reinterpret_cast<int*>(base + o_sc);
+  h->ws.trace = reinterpret_cast<unsigned long long*>(base + o_tr);
 
   cudaStream_t s = nullptr;
   if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess) {
@@ -336,11 +333,8 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   // The expert kernels run one CTA per SM with most of its shared memory;
   // asking for the largest carveout up front avoids a reconfiguration of the
   // L1/shared split between launches.
-  if ((e = cudaFuncSetAttribute(h->k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem1)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(h->k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem2)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(h->k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem3)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(h->k2, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(h->k3, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess) {
+  if ((e = cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem_max)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(h->kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess) {
     cuda_fail(e, "shared-memory attribute");
     free_layer(h);
     return nullptr;
@@ -358,6 +352,7 @@ int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, 
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool pdl = !(flags & MOE_FWD_NO_PDL);
+  const bool trace = (flags & MOE_FWD_TRACE) != 0;
   if (flags & MOE_FWD_GRAPH) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     cudaError_t e = cudaStreamIsCapturing(st, &cs);
@@ -369,7 +364,7 @@ int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, 
         cudaGraph_t g = nullptr;
         if ((e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
           return cuda_fail(e, "begin capture");
-        rc = launch_all(h, x, out, topk_idx, topk_w, M, h->cap_stream, pdl, nullptr);
+        rc = launch_layer(h, x, out, topk_idx, topk_w, M, h->cap_stream, pdl, trace, nullptr);
         e = cudaStreamEndCapture(h->cap_stream, &g);
         if (rc != MOE_OK) { if (g) cudaGraphDestroy(g); return rc; }
         if (e != cudaSuccess) return cuda_fail(e, "end capture");
@@ -392,7 +387,7 @@ int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, 
       return MOE_OK;
     }
   }
-  return launch_all(h, x, out, topk_idx, topk_w, M, st, pdl, nullptr);
+  return launch_layer(h, x, out, topk_idx, topk_w, M, st, pdl, trace, nullptr);
 }
 
 int moe_forward(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, int M, moe_stream_t stream) {
@@ -403,10 +398,10 @@ int moe_forward_timed(moe_layer_t* h, const void* x, void* out, int32_t* topk_id
                       moe_stream_t stream, moe_event_t* ev) {
   int rc = check_forward_args(h, x, out, topk_idx, M);
   if (rc != MOE_OK) return rc;
-  if (!ev || !ev[0] || !ev[1] || !ev[2] || !ev[3]) { set_err("need 4 events"); return MOE_ERR_INVALID_ARG; }
+  if (!ev || !ev[0] || !ev[1]) { set_err("need 2 events"); return MOE_ERR_INVALID_ARG; }
   if (M == 0) return MOE_OK;
-  return launch_all(h, x, out, topk_idx, nullptr, M, reinterpret_cast<cudaStream_t>(stream), false,
-                    reinterpret_cast<cudaEvent_t*>(ev));
+  return launch_layer(h, x, out, topk_idx, nullptr, M, reinterpret_cast<cudaStream_t>(stream), false, false,
+                      reinterpret_cast<cudaEvent_t*>(ev));
 }
 
 int moe_set_router_bias(moe_layer_t* h, const float* bias) {
@@ -444,12 +439,17 @@ int moe_get_status(moe_layer_t* h) {
   if (st) {
     cudaMemset(h->ws.status, 0, 4);
     cudaMemset(h->ws.diag, 0, sizeof dg);
-    set_err("device status bits 0x%x (1 stage wait, 2 free-stage wait, 4 reduction wait, 8 bad index); "
-            "first timeout: kernel %llu kind %llu cta %llu stages %llu index %llu waited %llu ns "
-            "barrier 0x%016llx thread %llu grid %llu",
+    // a wait that gave up may have left the grid-barrier count between two
+    // multiples of the grid: start it again from zero (no kernel runs now)
+    cudaMemset(h->ws.sync, 0, kSyncWords * 4);
+    set_err("device status bits 0x%x (1 stage wait, 2 free-stage wait, 4 reduction wait, 8 no top-k "
+            "candidate, 16 grid-wide wait); first timeout: phase %llu kind %llu cta %llu stages %llu "
+            "index %llu waited %llu ns barrier 0x%016llx thread %llu grid %llu",
             st, dg[0] >> 56, (dg[0] >> 48) & 0xff, (dg[0] >> 32) & 0xffff, (dg[0] >> 16) & 0xffff,
             dg[0] & 0xffff, dg[1], dg[2], dg[3] >> 32, dg[3] & 0xffffffffull);
-    return (st & 7) ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_CUDA;
+    return (st & (kErrTimeoutFull | kErrTimeoutEmpty | kErrTimeoutReduce | kErrTimeoutGrid))
+               ? MOE_ERR_DEVICE_TIMEOUT
+               : MOE_ERR_CUDA;
   }
   return MOE_OK;
 }
@@ -459,13 +459,15 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
   o->hidden = h->H; o->n_experts = h->E; o->topk = h->K; o->inter = h->I;
   o->max_tokens = MOE_MAX_TOKENS;
   o->n_sms = h->n_sms;
-  o->gateup_stages = h->s2;
-  o->down_stages = h->s3;
-  o->gateup_tile_bytes = (int)h->tile2;
-  o->down_tile_bytes = (int)h->tile3;
+  o->gateup_stages = h->s_gu;
+  o->down_stages = h->s_d;
+  o->gateup_tile_bytes = (int)h->tile_gu;
+  o->down_tile_bytes = (int)h->tile_d;
   o->weight_bytes = h->weight_bytes;
   o->workspace_bytes = h->ws_bytes;
-  o->kernels_per_forward = 3;
+  o->kernels_per_forward = 1;
+  o->router_split = h->ks;
+  o->smem_bytes = h->smem_max;
   return MOE_OK;
 }
 
@@ -493,6 +495,16 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active, int32_
   if (np > 0 && pair_w && (e = cudaMemcpy(pair_w, h->ws.pair_w, np * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "routing read");
   return MOE_OK;
+}
+
+int moe_read_trace(moe_layer_t* h, uint64_t* out, int cap) {
+  if (!h || !out || cap < 0) { set_err("bad argument"); return -MOE_ERR_INVALID_ARG; }
+  const int n = std::min(cap, h->n_sms * kTraceSlots);
+  cudaError_t e;
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return -cuda_fail(e, "synchronize");
+  if (n > 0 && (e = cudaMemcpy(out, h->ws.trace, (size_t)n * 8, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return -cuda_fail(e, "trace read");
+  return n;
 }
 
 void moe_destroy(moe_layer_t* h) {

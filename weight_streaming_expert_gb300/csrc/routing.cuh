@@ -1,0 +1,375 @@
+// routing.cuh -- the router of one call: gate matvec, softmax top-k with
+// renormalisation, and the token->expert compaction, as device functions
+// shared by the layer kernel and the allocation-free routing kernel.
+//
+// Method (page "How Ling-3.0-flash reduces batch 1 decoding latency by 54%
+// on 4 Blackwell GPUs"):
+//  * "bf16 router gate and lm_head": the gate weight is bf16 and pure
+//    bandwidth (2.6 MB per layer at hidden 2560 x 512 experts); logits and
+//    the softmax are fp32.
+//  * "PDL: the latency floor of stacked small kernels", Figure 7: the gate
+//    weight does not depend on the producer of x, so its load is issued
+//    before the dependency wait.
+//  * "Two fusions and a retune" (moe_align on the pair axis): the M*k
+//    (token, slot) pairs are bucketed by expert with a stable order inside a
+//    bucket, and the bucket offsets never leave the device.
+//
+// GB300 design.
+//  * Gate matvec on the tensor cores: a unit = 8 experts (n8) x 1/ks of the
+//    hidden dim; its 8 warps split that slice and every warp runs m16n8k16
+//    bf16 MMAs with the tokens as A (16 per pass) and the 8 weight rows as B.
+//    The weight keeps the caller's [E][H] layout: inside every 32-wide k
+//    chunk the MMA's logical k order is permuted so that lane (g, t) holds
+//    physical k = 8t .. 8t+7 of both operands, i.e. ONE 16-byte load per
+//    operand row per chunk (the same permutation on A and B leaves every dot
+//    product unchanged).  Units write fp32 partial logits; the reader sums
+//    the ks partials in a fixed order, so the logits are deterministic.
+//  * Top-k, one warp per token: the E logits sit in registers (lane l holds
+//    experts l + 32v as order-preserving integer keys); k rounds of a
+//    redux.sync arg-max (largest key; ties -- bit-equal logits -- to the
+//    lowest expert id), after which every lane re-reduces its own keys with
+//    a depth-log2 tree (branch-free).  Weights: exp(l_j - l_0) over the k
+//    chosen, normalised by their sum (= the full softmax renormalised over
+//    the k; its denominator cancels).
+//  * Compaction from bit masks: an expert is chosen at most once per token,
+//    so bit m of mask[e] says "token m chose e".  popc(mask[e]) is the
+//    bucket size and popc(mask[e] & (2^m - 1)) the pair's stable rank in its
+//    bucket -- every pair is placed independently, no serial pass.
+#pragma once
+
+#include "common.cuh"
+
+namespace wse {
+
+// ------------------------------------------------------- gate matvec ---
+struct GemvUnit {
+  int tile;  // experts [8 tile, 8 tile + 8)
+  int kc;    // hidden-dim slice index, 0..ks-1
+  int q0;    // first 32-wide k chunk of this warp
+  int nq;    // k chunks of this warp
+};
+
+__device__ __forceinline__ GemvUnit gemv_unit(int unit, int ks, int H, int warp) {
+  GemvUnit u;
+  u.tile = unit / ks;
+  u.kc = unit - u.tile * ks;
+  const int per_unit = (H / 32) / ks;
+  u.nq = per_unit / kConsumerWarps;
+  u.q0 = u.kc * per_unit + warp * u.nq;
+  return u;
+}
+
+// B fragments of this warp's slice (rows past E repeat the last row; their
+// results are never stored).  KPW = H / 256 >= nq.
+template <int KPW>
+__device__ __forceinline__ void gemv_load_w(const __nv_bfloat16* __restrict__ w_router, int E, int H,
+                                            const GemvUnit& u, int lane, uint4 (&b)[KPW]) {
+  const int row = min(u.tile * 8 + (lane >> 2), E - 1);
+  const uint4* src = reinterpret_cast<const uint4*>(w_router + (size_t)row * H) + (lane & 3);
+#pragma unroll
+  for (int q = 0; q < KPW; ++q)
+    if (q < u.nq) b[q] = __ldg(src + 4 * (u.q0 + q));
+}
+
+// This warp's partial (tokens 16 mb + g, 16 mb + g + 8) x (experts 2t, 2t+1
+// of the tile) over its k slice, as (c0, c1, c2, c3) of the m16n8 C tile.
+template <int KPW>
+__device__ __forceinline__ float4 gemv_tokens(const __nv_bfloat16* __restrict__ x, int M, int H,
+                                              const GemvUnit& u, int mb, int lane,
+                                              const uint4 (&b)[KPW]) {
+  const int g4 = lane >> 2, t4 = lane & 3;
+  const int m0 = min(mb * 16 + g4, M - 1), m1 = min(mb * 16 + g4 + 8, M - 1);
+  const uint4* x0 = reinterpret_cast<const uint4*>(x + (size_t)m0 * H) + t4;
+  const uint4* x1 = reinterpret_cast<const uint4*>(x + (size_t)m1 * H) + t4;
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < KPW; ++q) {
+    if (q < u.nq) {
+      const uint4 xa = x0[4 * (u.q0 + q)], xb = x1[4 * (u.q0 + q)];
+      // logical k (2t, 2t+1 | 2t+8, 2t+9) of step 0 = physical 8t + (0,1 | 2,3);
+      // step 1 takes physical 8t + (4,5 | 6,7)
+      mma_bf16(c0, xa.x, xb.x, xa.y, xb.y, b[q].x, b[q].y);
+      mma_bf16(c1, xa.z, xb.z, xa.w, xb.w, b[q].z, b[q].w);
+    }
+  }
+  return make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
+}
+
+// Warp 0 of the unit's CTA: sum the 8 warp partials in warp order and store
+// the unit's fp32 partial logits part[kc][m][e] (plane = rows * E floats).
+__device__ __forceinline__ void gemv_store(const float4* red, const GemvUnit& u, int mb, int M, int E,
+                                           size_t plane, float* __restrict__ part, int lane) {
+  float4 s = red[lane];
+#pragma unroll
+  for (int w = 1; w < kConsumerWarps; ++w) {
+    const float4 v = red[w * 32 + lane];
+    s.x += v.x;
+    s.y += v.y;
+    s.z += v.z;
+    s.w += v.w;
+  }
+  const int e = u.tile * 8 + 2 * (lane & 3);
+  const int m0 = mb * 16 + (lane >> 2), m1 = m0 + 8;
+  float* P = part + (size_t)u.kc * plane;
+  if (m0 < M) {
+    if (e < E) P[(size_t)m0 * E + e] = s.x;
+    if (e + 1 < E) P[(size_t)m0 * E + e + 1] = s.y;
+  }
+  if (m1 < M) {
+    if (e < E) P[(size_t)m1 * E + e] = s.z;
+    if (e + 1 < E) P[(size_t)m1 * E + e + 1] = s.w;
+  }
+}
+
+// Largest divisor ks of H/256 with ceil(E/8) * ks <= units_max (>= 1).
+__host__ __device__ inline int gemv_split(int H, int E, int units_max) {
+  const int kpw = H / 256, tiles = (E + 7) / 8;
+  int best = 1;
+  for (int ks = 1; ks <= kpw; ++ks)
+    if (kpw % ks == 0 && tiles * ks <= units_max) best = ks;
+  return best;
+}
+
+// ------------------------------------------------------------ top-k ----
+// Order-preserving map of a float to an unsigned key (larger float ->
+// larger key).  Key 0 marks "taken / no expert"; every float maps to >= 1
+// (only two NaN encodings share key 1), so a candidate always remains
+// while fewer than E experts have been taken.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return k > 1u ? k : 1u;
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Arg-max of key[0..VPL) by a tree (ties keep the lower index).
+template <int VPL>
+__device__ __forceinline__ void tree_argmax(const uint32_t (&key)[VPL], uint32_t& best, int& bv) {
+  uint32_t tk[VPL];
+  int tv[VPL];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    tk[v] = key[v];
+    tv[v] = v;
+  }
+#pragma unroll
+  for (int s = 1; s < VPL; s <<= 1) {
+#pragma unroll
+    for (int v = 0; v + s < VPL; v += 2 * s) {
+      if (tk[v + s] > tk[v]) {
+        tk[v] = tk[v + s];
+        tv[v] = tv[v + s];
+      }
+    }
+  }
+  best = tk[0];
+  bv = tv[0];
+}
+
+// Top-k of one token by one warp.  lg: the token's partial logits (plane 0;
+// ks planes `plane` floats apart), summed in plane order, plus the bias.
+// Lane j < K writes slot j's expert id to idx_out[j] (the caller reads them
+// after a __syncwarp) and returns slot j's renormalised weight; the other
+// lanes return 0.  A round: redux.sync max of the lane bests, redux.sync min
+// of the ids holding it (ties -- bit-equal logits -- to the lowest id; inside
+// a lane the tree keeps the lower index, i.e. the lower id), then every lane
+// drops the winner if it holds it and re-reduces with the tree.
+template <int VPL>
+__device__ float topk_token(const float* __restrict__ lg, size_t plane, int ks,
+                            const float* __restrict__ bias, int E, int K, int lane, int* status,
+                            int* idx_out) {
+  // planes 0 and 1 and the bias in one round trip; further planes one each;
+  // the sum order is plane 0, 1, ..., then the bias
+  float lv[VPL], l1[VPL], bv_[VPL];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = v * 32 + lane;
+    lv[v] = e < E ? __ldcg(lg + e) : 0.f;
+    l1[v] = (ks > 1 && e < E) ? __ldcg(lg + plane + e) : 0.f;
+    bv_[v] = (bias && e < E) ? __ldg(bias + e) : 0.f;
+  }
+  if (ks > 1) {
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) lv[v] += l1[v];
+  }
+  for (int c = 2; c < ks; ++c) {
+    float pv[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const int e = v * 32 + lane;
+      pv[v] = e < E ? __ldcg(lg + (size_t)c * plane + e) : 0.f;
+    }
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) lv[v] += pv[v];
+  }
+  uint32_t key[VPL];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = v * 32 + lane;
+    if (bias) lv[v] += bv_[v];
+    key[v] = e < E ? ordered_key(lv[v]) : 0u;
+  }
+  uint32_t best;
+  int bv;
+  tree_argmax<VPL>(key, best, bv);
+
+  // branch-free rounds: a divergent winner-only update costs more than the
+  // second redux and the all-lane rescan it would save
+  uint32_t my_key = 0u;
+  for (int j = 0; j < K; ++j) {
+    const uint32_t top = __reduce_max_sync(0xffffffffu, best);
+    const uint32_t cand = (best == top) ? (uint32_t)(bv * 32 + lane) : 0xffffffffu;
+    uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    if (top == 0u || win >= (uint32_t)E) {  // unreachable while K <= E
+      if (lane == 0) set_error(status, kErrBadIndex);
+      win = 0;
+    }
+    if (lane == j) {
+      my_key = top;
+      idx_out[j] = (int)win;
+    }
+    const bool mine = (int)(win & 31u) == lane;
+    const int wv = (int)(win >> 5);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) key[v] = (mine && v == wv) ? 0u : key[v];
+    tree_argmax<VPL>(key, best, bv);
+  }
+  // weights: exp(l_j - l_0), normalised by a fixed butterfly sum
+  const float my_val = key_value(my_key);
+  const float v0 = __shfl_sync(0xffffffffu, my_val, 0);
+  const float ex = lane < K ? expf(my_val - v0) : 0.f;
+  float s = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return lane < K ? ex / s : 0.f;
+}
+
+__device__ __forceinline__ float topk_dispatch(const float* lg, size_t plane, int ks, const float* bias,
+                                               int E, int K, int lane, int* status, int* idx_out) {
+  if (E <= 32) return topk_token<1>(lg, plane, ks, bias, E, K, lane, status, idx_out);
+  if (E <= 64) return topk_token<2>(lg, plane, ks, bias, E, K, lane, status, idx_out);
+  if (E <= 128) return topk_token<4>(lg, plane, ks, bias, E, K, lane, status, idx_out);
+  if (E <= 256) return topk_token<8>(lg, plane, ks, bias, E, K, lane, status, idx_out);
+  if (E <= 512) return topk_token<16>(lg, plane, ks, bias, E, K, lane, status, idx_out);
+  return topk_token<32>(lg, plane, ks, bias, E, K, lane, status, idx_out);
+}
+
+// ------------------------------------------------------- compaction ----
+// Shared-memory routing of one call (ints unless noted):
+//   mask[E] (u64)  s_off[E]  s_e[NP]  s_w[NP] (float)  pair_list[NP]
+//   grp_expert[NP]  grp_start[NP]  grp_cnt[NP]  scal[96]
+// (the compaction comment in the header says how the positions are found)
+__host__ __device__ inline size_t routing_smem_bytes(int NP, int E) {
+  return (size_t)E * 8 + (size_t)E * 4 + (size_t)NP * 4 * 6 + 96 * 4;
+}
+
+struct SmemRouting {
+  unsigned long long* mask;
+  int* s_off;
+  int* s_e;         // [NP] expert of pair p = token * K + slot
+  float* s_w;       // [NP] routing weight of pair p
+  int* pair_list;   // [NP] pair id at each sorted position
+  int* grp_expert;  // [groups] expert of each group (ascending expert id)
+  int* grp_start;   // [groups] first sorted position
+  int* grp_cnt;     // [groups] pairs in the group (1..16)
+  int* scal;        // [0] groups, [1] distinct experts, [8..88) scan scratch
+};
+
+__device__ __forceinline__ SmemRouting routing_carve(uint8_t* base, int NP, int E) {
+  SmemRouting r;
+  r.mask = reinterpret_cast<unsigned long long*>(base);
+  r.s_off = reinterpret_cast<int*>(r.mask + E);
+  r.s_e = r.s_off + E;
+  r.s_w = reinterpret_cast<float*>(r.s_e + NP);
+  r.pair_list = reinterpret_cast<int*>(r.s_w + NP);
+  r.grp_expert = r.pair_list + NP;
+  r.grp_start = r.grp_expert + NP;
+  r.grp_cnt = r.grp_start + NP;
+  r.scal = r.grp_cnt + NP;
+  return r;
+}
+
+// Cooperative over the CTA; mask[] and s_e[] complete and visible (a
+// __syncthreads() before).  Bucket sizes and group counts by a block-wide
+// scan over the experts; every pair then takes its place independently.
+// Ends with a __syncthreads().
+__device__ inline void compact_masks(const SmemRouting& r, int M, int K, int E) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int NP = M * K;
+  // (pairs << 16) + groups share one int (both <= 2048, no carry)
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+  int* s_wt = r.scal + 8;
+  int* s_wa = r.scal + 48;
+  const int per = (E + nt - 1) / nt;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int packed = 0, act = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = __popcll(r.mask[e]);
+    packed += (c << 16) + (c + kGroupTokens - 1) / kGroupTokens;
+    act += c > 0;
+  }
+  int inc = packed, ainc = act;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    const int ta = __shfl_up_sync(0xffffffffu, ainc, o);
+    if (lane >= o) {
+      inc += t;
+      ainc += ta;
+    }
+  }
+  if (lane == 31) {
+    s_wt[warp] = inc;
+    s_wa[warp] = ainc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < nwarps ? s_wt[lane] : 0;
+    int va = lane < nwarps ? s_wa[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      const int ta = __shfl_up_sync(0xffffffffu, va, o);
+      if (lane >= o) {
+        v += t;
+        va += ta;
+      }
+    }
+    if (lane < nwarps) {
+      s_wt[lane] = v;
+      s_wa[lane] = va;
+    }
+    if (lane == nwarps - 1) {
+      r.scal[0] = v & 0xffff;
+      r.scal[1] = va;
+    }
+  }
+  __syncthreads();
+  {
+    const int base = (warp > 0 ? s_wt[warp - 1] : 0) + inc - packed;
+    int c_off = base >> 16, g_off = base & 0xffff;
+    for (int e = e0; e < e1; ++e) {
+      const int c = __popcll(r.mask[e]);
+      r.s_off[e] = c_off;
+      for (int q = 0; q * kGroupTokens < c; ++q) {
+        const int g = g_off + q;
+        r.grp_expert[g] = e;
+        r.grp_start[g] = c_off + q * kGroupTokens;
+        r.grp_cnt[g] = min(kGroupTokens, c - q * kGroupTokens);
+      }
+      c_off += c;
+      g_off += (c + kGroupTokens - 1) / kGroupTokens;
+    }
+  }
+  __syncthreads();
+  for (int p = tid; p < NP; p += nt) {
+    const int e = r.s_e[p], m = p / K;
+    const int rank = __popcll(r.mask[e] & ((1ull << m) - 1ull));
+    r.pair_list[r.s_off[e] + rank] = p;
+  }
+  __syncthreads();
+}
+
+}  // namespace wse

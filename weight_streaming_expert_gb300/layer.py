@@ -62,7 +62,8 @@ class MoELayer:
         N.check("moe_set_router_bias", N.lib().moe_set_router_bias(self._h, _ptr(bias)))
         torch.cuda.synchronize(self.device)
 
-    def forward(self, x, out=None, topk_idx=None, topk_w=None, stream=None, pdl=True, graph=False):
+    def forward(self, x, out=None, topk_idx=None, topk_w=None, stream=None, pdl=True, graph=False,
+                trace=False):
         """x: bf16 [M, H] CUDA.  Returns (out [M,H] bf16, topk_idx [M,k] int32)."""
         M = x.shape[0]
         if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.shape[1] != self.hidden:
@@ -71,7 +72,8 @@ class MoELayer:
             out = torch.empty_like(x)
         if topk_idx is None:
             topk_idx = torch.empty((M, self.topk), dtype=torch.int32, device=x.device)
-        flags = (0 if pdl else N.MOE_FWD_NO_PDL) | (N.MOE_FWD_GRAPH if graph else 0)
+        flags = ((0 if pdl else N.MOE_FWD_NO_PDL) | (N.MOE_FWD_GRAPH if graph else 0)
+                 | (N.MOE_FWD_TRACE if trace else 0))
         rc = N.lib().moe_forward_ex(self._h, _ptr(x), _ptr(out), _ptr(topk_idx), _ptr(topk_w), M,
                                     _stream_ptr(stream), flags)
         N.check("moe_forward_ex", rc)
@@ -80,15 +82,26 @@ class MoELayer:
     __call__ = forward
 
     def forward_timed(self, x, out, topk_idx, events, stream=None):
-        """Profiling launch: events = 4 torch.cuda.Event(enable_timing=True)."""
+        """Profiling launch: events = 2 torch.cuda.Event(enable_timing=True)."""
         st = stream if stream is not None else torch.cuda.current_stream()
         for e in events:
             if not e.cuda_event:      # torch creates the CUDA event on first record
                 e.record(st)
-        arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        arr = (ctypes.c_void_p * 2)(*[ctypes.c_void_p(e.cuda_event) for e in events[:2]])
         rc = N.lib().moe_forward_timed(self._h, _ptr(x), _ptr(out), _ptr(topk_idx), x.shape[0],
                                        _stream_ptr(stream), arr)
         N.check("moe_forward_timed", rc)
+
+    def read_trace(self):
+        """Phase timestamps of the last traced call: int64 numpy [SMs, 16] (ns;
+        slot 11 is the CTA's gate/up tile count).  Synchronises."""
+        import numpy as np
+        n = self.info().n_sms * N.TRACE_SLOTS
+        buf = np.zeros(n, np.uint64)
+        rc = N.lib().moe_read_trace(self._h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), n)
+        if rc < 0:
+            N.check("moe_read_trace", -rc)
+        return buf.astype(np.int64).reshape(-1, N.TRACE_SLOTS)
 
     def status(self) -> int:
         """Synchronises; returns the sticky device status (0 = ok) and clears it."""

@@ -24,6 +24,8 @@ MOE_ERR_DEVICE_TIMEOUT = 5
 MOE_MAX_TOKENS = 64
 MOE_FWD_NO_PDL = 0x1
 MOE_FWD_GRAPH = 0x2
+MOE_FWD_TRACE = 0x4
+TRACE_SLOTS = 32
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
                 4: "MOE_ERR_OOM", 5: "MOE_ERR_DEVICE_TIMEOUT"}
@@ -35,7 +37,8 @@ class moe_info_t(ctypes.Structure):
                 ("gateup_stages", ctypes.c_int), ("down_stages", ctypes.c_int),
                 ("gateup_tile_bytes", ctypes.c_int), ("down_tile_bytes", ctypes.c_int),
                 ("weight_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
-                ("kernels_per_forward", ctypes.c_int)]
+                ("kernels_per_forward", ctypes.c_int), ("router_split", ctypes.c_int),
+                ("smem_bytes", ctypes.c_size_t)]
 
 
 class MoEError(RuntimeError):
@@ -80,6 +83,10 @@ def lib(build_if_missing: bool = True):
         L.moe_get_info.restype = ci
         L.moe_read_routing.argtypes = [vp, ci, ip, ip, i32p, i32p, i32p, i32p, f32p, ci]
         L.moe_read_routing.restype = ci
+        L.moe_read_trace.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64), ci]
+        L.moe_read_trace.restype = ci
+        L.moe_route_static.argtypes = [ci, ci, ci, vp, vp, vp, ci, vp, vp, vp]
+        L.moe_route_static.restype = ci
         L.moe_destroy.argtypes = [vp]
         L.moe_destroy.restype = None
         L.moe_last_error.argtypes = []
