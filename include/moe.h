@@ -87,7 +87,8 @@ typedef enum {
  *              {1,2,4,5,8,10,12,16}; (2560 = Ling-3.0-flash width).
  *   n_experts  E: routed experts, topk <= E <= 1024.
  *   topk       k: experts per token, 1 <= k <= 32.
- *   inter      I: expert intermediate width, one of {128, 256, 512}.
+ *   inter      I: expert intermediate width, one of {128, 256, 512},
+ *              dividing hidden.
  *   w_router   device bf16 [E][H], row e = router row of expert e
  *              (the hidden -> n_experts mapping, stored one row per expert).
  *              All three weight pointers must be 16-byte aligned.
@@ -178,7 +179,8 @@ typedef struct {
   int gateup_stages;       /* shared-memory ring depth of the gate/up phase */
   int down_stages;         /* shared-memory stages of the down phase */
   int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 rows x H) */
-  int down_tile_bytes;     /* bytes of one down weight tile (8 rows x I) */
+  int down_tile_bytes;     /* bytes of one down super tile (8 slabs of
+                              8 rows x I, one per consumer warp) */
   size_t weight_bytes;     /* device bytes held for the weights */
   size_t workspace_bytes;  /* device bytes held for the workspace */
   int kernels_per_forward; /* kernel launches per forward call (1) */

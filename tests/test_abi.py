@@ -26,7 +26,7 @@ def L():
     return native.lib()
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_layer_calls():
     names = declared_functions()
     for n in ("moe_create", "moe_forward", "moe_destroy"):
         assert n in names
@@ -48,6 +48,8 @@ def test_built_for_sm103a_only():
     ((255, 512, 8, 512), "hidden"),
     ((2560 + 256, 512, 8, 512), "hidden"),   # 11 x 256: no kernel instantiation
     ((2560, 512, 8, 384), "inter"),
+    ((256, 16, 2, 512), "inter"),            # inter not dividing hidden
+    ((1280, 40, 2, 512), "inter"),
     ((2560, 512, 0, 512), "topk"),
     ((2560, 512, 33, 512), "topk"),
     ((2560, 4, 8, 512), "n_experts"),

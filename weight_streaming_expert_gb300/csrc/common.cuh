@@ -21,7 +21,7 @@ constexpr int kExpertThreads = (kConsumerWarps + 2) * 32;
 constexpr int kGateUpTileRows = 8;    // 4 gate rows interleaved with their 4 up rows
 constexpr int kDownTileRows = 8;      // 8 output rows (n8) x I per down tile
 constexpr int kMaxGateUpStages = 7;   // < 8 reduction slots: see the reduction-slot argument
-constexpr int kMaxDownStages = 8;     // down stages of 8 slabs (one per consumer warp)
+constexpr int kMaxDownStages = 8;     // down slots (ring regions of one 8-slab super tile)
 constexpr int kMaxDownChunks = 16;    // 32-wide k chunks of a down row: I <= 512
 constexpr uint32_t kBulkChunk = 16384;  // bytes per cp.async.bulk
 constexpr int kTraceSlots = 32;       // per-CTA phase timestamps of a traced call

@@ -21,15 +21,11 @@ struct LayerArgs {
   int M, H, E, K, I;
   int ks;                         // hidden-dim split of the router matvec
   int gu_stages;                  // gate/up ring depth
-  int d_stages;                   // down stages, a multiple of 8
+  int d_stages;                   // down slots of one super tile (8 slabs) each
   uint32_t gu_tile;               // 8 rows x H x 2 bytes
   uint32_t d_tile;                // 8 rows x I x 2 bytes
-  uint32_t ring_bytes;            // max(gu_stages*gu_tile + reduction area, d_stages*d_tile)
+  uint32_t ring_bytes;            // gu_stages*gu_tile + the reduction area
   int trace;                      // record phase timestamps
-  // per down stage: bit s = the stage's bytes overlap gate/up stage s, bit
-  // 31 = they overlap the reduction area (a pure function of the four sizes
-  // above, computed at create)
-  uint32_t d_need[kMaxDownStages];
   Workspace ws;
 };
 

@@ -69,26 +69,31 @@ namespace wse {
 namespace layer_detail {
 
 // shared-memory map (bytes)
-constexpr uint32_t kOffFull = 0;     // [8] gate/up stage: data landed (1 arrival + tx)
-constexpr uint32_t kOffEmpty = 64;   // [8] gate/up stage: read by the 8 consumer warps
-constexpr uint32_t kOffReady = 128;  // [8] gate/up stage: tile id written (1 arrival)
-constexpr uint32_t kOffRedBar = 192; // [8] reduction slot: 8 partials written
-constexpr uint32_t kOffDone = 256;   // [1] all consumer warps left the gate/up loop
-constexpr uint32_t kOffStatic = 520; // [1] all consumer warps reduced the static gate/up tiles
-constexpr uint32_t kOffLevel1 = 528;  // [1] every CTA's static gate/up tiles reduced (publisher)
-constexpr uint32_t kOffLevel2 = 536;  // [1] every CTA's gate/up tiles reduced (publisher)
-constexpr uint32_t kOffCall = 544;    // u64: the call's index on the grid counters (1, 2, ...)
-constexpr uint32_t kOffDFull = 264;  // [8] down stage: data landed (1 arrival + tx)
-constexpr uint32_t kOffDEmpty = 328; // [8] down stage: read by the 8 consumer warps
-constexpr uint32_t kOffDReady = 392; // [8] down stage: super-tile id written (1 arrival)
-constexpr uint32_t kOffTile = 456;   // [8] int: tile id in each gate/up stage (-1: no more)
-constexpr uint32_t kOffDTile = 488;  // [8] int: super-tile id in each down stage (-1: no more)
-constexpr uint32_t kRingOff = 1024;
+constexpr uint32_t kOffFull = 0;      // [8] gate/up stage: data landed (1 arrival + tx)
+constexpr uint32_t kOffEmpty = 64;    // [8] gate/up stage: read by the 8 consumer warps
+constexpr uint32_t kOffReady = 128;   // [8] gate/up stage: tile id written (1 arrival)
+constexpr uint32_t kOffRedBar = 192;  // [8] reduction slot: 8 partials written
+constexpr uint32_t kOffDone = 256;    // [1] all consumer warps left the gate/up loop
+constexpr uint32_t kOffStatic = 264;  // [1] all consumer warps reduced the static gate/up tiles
+constexpr uint32_t kOffLevel1 = 272;  // [1] every CTA's static gate/up tiles reduced (publisher)
+constexpr uint32_t kOffLevel2 = 280;  // [1] every CTA's gate/up tiles reduced (publisher)
+constexpr uint32_t kOffCall = 288;    // u64: the call's index on the grid counters (1, 2, ...)
+constexpr uint32_t kOffTile = 336;    // [8] int: tile id in each gate/up stage (-1: no more)
+constexpr uint32_t kOffDTile = 384;   // [8] int: super-tile id in each down slot (-1: no more)
+constexpr uint32_t kOffDFull = 416;   // [8] down slot: data landed (1 arrival + tx)
+constexpr uint32_t kOffDEmpty = 480;  // [8] down slot: read by the 8 consumer warps
+constexpr uint32_t kOffDReady = 544;  // [8] down slot: super-tile id written (1 arrival)
+constexpr uint32_t kOffCells = 608;   // [8][8] int: ring cell of (down slot, consumer warp)
+constexpr uint32_t kRingOff = 896;
 constexpr int kRedSlots = 8;
 constexpr uint32_t kRedBytes = kRedSlots * kConsumerWarps * 32 * 16;
 constexpr int kStaticNum = 3, kStaticDen = 4;  // statically split share of the groups
-static_assert(kMaxDownStages <= 8 && kMaxGateUpStages <= 8, "barrier map");
-static_assert(kOffDTile + 4 * kMaxDownStages <= kOffStatic && kOffCall + 8 <= kRingOff, "map");
+static_assert(kMaxGateUpStages <= 8 && kMaxDownStages <= 8, "barrier map");
+static_assert(kOffCall + 8 <= kOffTile && kOffTile + 4 * kMaxGateUpStages <= kOffDTile &&
+                  kOffDReady + 8 * kMaxDownStages <= kOffCells &&
+                  kOffCells + 4 * kMaxDownStages * kConsumerWarps <= kRingOff,
+              "map");
+static_assert(kRingOff % 128 == 0, "ring alignment");
 static_assert(kMaxGateUpStages < kRedSlots, "reduction slots must outnumber ring stages");
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -165,12 +170,14 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) stamp(a, 19);  // CTA started
-  const int S = a.gu_stages, SD = a.d_stages;
+  const int S = a.gu_stages;
+  const int NSL = kConsumerWarps, SD = a.d_stages;  // slabs per down super tile, down slots
   const int NP = a.M * a.K;
   const uint32_t sb = smem_u32(smem);
   int* stage_tile = reinterpret_cast<int*>(smem + kOffTile);
   int* dstage_tile = reinterpret_cast<int*>(smem + kOffDTile);
-  const uint32_t dsuper = kConsumerWarps * a.d_tile;  // bytes of a down stage
+  const uint32_t dsuper = (uint32_t)NSL * a.d_tile;  // bytes of a down super tile
+  int* cell_tab = reinterpret_cast<int*>(smem + kOffCells);  // [slot][warp] -> ring cell
   uint8_t* ring = smem + kRingOff;
   const uint32_t ring_u32 = sb + kRingOff;
   float4* red = reinterpret_cast<float4*>(ring + (size_t)S * a.gu_tile);
@@ -186,6 +193,13 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   const uint32_t static_bar = sb + kOffStatic;
   const uint32_t level1 = sb + kOffLevel1, level2 = sb + kOffLevel2;
   unsigned long long* call_idx = reinterpret_cast<unsigned long long*>(smem + kOffCall);
+
+  // ---- 1. producer-independent: this CTA's slice of the router weight
+  const int units = ((a.E + 7) / 8) * a.ks;
+  const int gw = warp < kConsumerWarps ? warp : 0;
+  GemvUnit gu = gemv_unit(blockIdx.x, a.ks, a.H, gw);
+  uint4 wb[KPW];
+  if ((int)blockIdx.x < units && warp < kConsumerWarps) gemv_load_w<KPW>(a.w_router, a.E, a.H, gu, lane, wb);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -208,13 +222,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   for (int e = tid; e < a.E; e += kExpertThreads) rt.mask[e] = 0ull;
   for (int p = tid; p < NP; p += kExpertThreads) rt.pair_list[p] = 0;
   if (tid < 2) rt.scal[tid] = 0;
-
-  // ---- 1. producer-independent: this CTA's slice of the router weight
-  const int units = ((a.E + 7) / 8) * a.ks;
-  const int gw = warp < kConsumerWarps ? warp : 0;
-  GemvUnit gu = gemv_unit(blockIdx.x, a.ks, a.H, gw);
-  uint4 wb[KPW];
-  if ((int)blockIdx.x < units && warp < kConsumerWarps) gemv_load_w<KPW>(a.w_router, a.E, a.H, gu, lane, wb);
 
   if (tid == 0) stamp(a, 20);  // prologue done
   pdl_wait();               // x and the workspace belong to this call now
@@ -290,12 +297,27 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   const int TPG = 2 * a.I / kGateUpTileRows;  // gate/up tiles per group
   const int T_gu = n_groups * TPG;
   const int SL = a.H / kDownTileRows;         // 8-row output slabs per group
-  const int SPG = SL / kConsumerWarps;        // down super tiles per group
+  const int SPG = SL / NSL;                   // down super tiles per group
   const int T_d = n_groups * SPG;
   // groups [0, g_static) are split statically in both GEMVs: their gate/up
   // tiles are all in the static share, and so are their down tiles
   const int g_static = n_groups * kStaticNum / kStaticDen;
-
+  // The down phase reuses the ring as cells of one slab (d_tile bytes; a
+  // gate/up stage is exactly cps cells, the reduction area behind the
+  // stages holds the rest).  Gate/up stage (n_gu + r) mod S is released for
+  // the last time r-th (n_gu = this CTA's gate/up tile count; stages it
+  // never used come first), the reduction area after all of them.  Listing
+  // the cells in that order, down slot u takes list entries 8u .. 8u + 7,
+  // one per consumer warp: its first use waits only for the releases that
+  // free those cells, and every cell of the ring is used.
+  // The producer writes the (slot, warp) -> cell table once, before its
+  // first down tile is handed out (the consumers read it after that).
+  const int cps = (int)(a.gu_tile / a.d_tile);
+  const int gu_cells = S * cps;
+  auto slot_rank = [&](int u) -> int {  // release index that frees slot u's last cell (S: reduction area)
+    const int p = u * kConsumerWarps + kConsumerWarps - 1;
+    return p < gu_cells ? p / cps : S;
+  };
   if (warp == kPublisherWarp) {
     // =============================================================== publisher
     if (lane != 0) return;
@@ -336,17 +358,20 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int q1 = (int)((long long)Ts2 * (blockIdx.x + 1) / gridDim.x);
     unsigned* next_gu = a.ws.sync + kSyncGateUpNext;
     unsigned* next_d = a.ws.sync + kSyncDownNext;
-    // one tile of each shared tail, taken early so the round trip is hidden
-    int dyn_gu = Ts + (int)atomicAdd(next_gu, 1u);
-    int dyn_d = Ts2 + (int)atomicAdd(next_d, 1u);
+    // tiles of the shared tails are taken one ahead (the atomic's round trip
+    // hides behind a tile), starting one tile before the static share ends:
+    // a tile taken earlier would be held back from faster SMs
+    const int n_s = s1 - s0, n_s2 = q1 - q0;
+    int dyn_gu = n_s <= 1 ? Ts + (int)atomicAdd(next_gu, 1u) : 0;
     bool ok = true;
     int level = 0;  // readiness of the h rows seen so far (see the publisher)
     // ---- gate/up tiles
     int j = 0;
     for (;; ++j) {
       int tile;
-      if (s0 + j < s1) {
+      if (j < n_s) {
         tile = s0 + j;
+        if (j == n_s - 2) dyn_gu = Ts + (int)atomicAdd(next_gu, 1u);
       } else {
         tile = dyn_gu;
         if (tile < T_gu) dyn_gu = Ts + (int)atomicAdd(next_gu, 1u);
@@ -389,45 +414,50 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       level = need;
       return true;
     };
-    // ---- down super tiles.  The first use of a down stage waits until the
-    // ring bytes under it are free: the gate/up stages there consumed for
-    // the last time (taken in consumption order), and for bytes over the
-    // reduction area, every consumer warp out of the gate/up loop.
-    uint32_t released = 0u;
-    for (int s = 0; s < S; ++s)
-      if (s >= n_gu) released |= 1u << s;
-    int r = 0;
-    bool done_seen = false;
-    auto release_until = [&](uint32_t need) -> bool {
-      while ((released & need) != need) {
-        if (r < S) {
-          const int jf = n_gu - S + r++;
-          if (jf < 0) continue;
-          const int s = jf % S;
-          if (!mbar_wait(empty(s), (jf / S) & 1, &waited)) {
-            record_timeout(a.ws, 3, kErrTimeoutEmpty, jf, S, empty(s), waited);
-            return false;
-          }
-          released |= 1u << s;
-        } else if (!done_seen) {
-          if (!mbar_wait(done, 0, &waited)) {
-            record_timeout(a.ws, 3, kErrTimeoutEmpty, -1, S, done, waited);
-            return false;
-          }
-          fence_proxy_async_smem();  // the reduction area was last written with ordinary stores
-          released = 0xffffffffu;
-          done_seen = true;
-        } else {
+    // ---- down super tiles.  Slot u's first use waits until its cells are
+    // free: the gate/up stages under them released for the last time (the
+    // last S gate/up tiles, in consumption order), and for cells over the
+    // reduction area every consumer warp out of the gate/up loop.
+    {  // list position p -> cell, by running counters (no division per entry)
+      int st = n_gu % S, within = 0;
+      for (int p = 0; p < SD * kConsumerWarps; ++p) {
+        cell_tab[p] = p >= gu_cells ? p : st * cps + within;
+        if (++within == cps) {
+          within = 0;
+          st = st + 1 == S ? 0 : st + 1;
+        }
+      }
+    }
+    int r_done = 0;  // gate/up final releases waited for
+    bool red_free = false;
+    auto release_until = [&](int rank) -> bool {
+      const int upto = rank < S ? rank : S - 1;
+      for (; r_done <= upto; ++r_done) {
+        const int jf = n_gu - S + r_done;
+        if (jf < 0) continue;  // a stage this CTA never used
+        const int st = jf % S;
+        if (!mbar_wait(empty(st), (jf / S) & 1, &waited)) {
+          record_timeout(a.ws, 3, kErrTimeoutEmpty, jf, S, empty(st), waited);
           return false;
         }
       }
+      if (rank >= S && !red_free) {
+        if (!mbar_wait(done, 0, &waited)) {
+          record_timeout(a.ws, 3, kErrTimeoutEmpty, -1, S, done, waited);
+          return false;
+        }
+        fence_proxy_async_smem();  // the reduction area was last written with ordinary stores
+        red_free = true;
+      }
       return true;
     };
+    int dyn_d = n_s2 <= 1 ? Ts2 + (int)atomicAdd(next_d, 1u) : 0;
     int j2 = 0;
     for (; ok; ++j2) {
       int tile;
-      if (q0 + j2 < q1) {
+      if (j2 < n_s2) {
         tile = q0 + j2;
+        if (j2 == n_s2 - 2) dyn_d = Ts2 + (int)atomicAdd(next_d, 1u);
       } else {
         tile = dyn_d;
         if (tile < T_d) dyn_d = Ts2 + (int)atomicAdd(next_d, 1u);
@@ -435,7 +465,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       if (tile >= T_d) break;
       const int s = j2 % SD;
       if (j2 < SD) {
-        if (!release_until(a.d_need[s])) {
+        if (!release_until(slot_rank(s))) {
           ok = false;
           break;
         }
@@ -448,9 +478,17 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       // group's h rows are ready
       const int g = tile / SPG, q = tile - g * SPG;
       mbar_arrive_expect_tx(dfull(s), dsuper);
-      bulk_g2s_chunked(ring_u32 + (uint32_t)s * dsuper,
-                       a.w_down + ((size_t)rt.grp_expert[g] * SL + (size_t)q * kConsumerWarps) * a.d_tile,
-                       dsuper, dfull(s));
+      {  // the 8 slabs are contiguous in global memory; one copy per run of adjacent cells
+        const uint8_t* src = a.w_down + ((size_t)rt.grp_expert[g] * SL + (size_t)q * NSL) * a.d_tile;
+        const int* cells = cell_tab + s * kConsumerWarps;
+        int w0 = 0;
+        for (int w = 1; w <= NSL; ++w) {
+          if (w < NSL && cells[w] == cells[w - 1] + 1) continue;
+          bulk_g2s_chunked(ring_u32 + (uint32_t)cells[w0] * a.d_tile, src + (size_t)w0 * a.d_tile,
+                           (uint32_t)(w - w0) * a.d_tile, dfull(s));
+          w0 = w;
+        }
+      }
       if (!ensure_ready(g)) {
         ok = false;
         break;
@@ -584,7 +622,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       const int tile = dstage_tile[s];
       if (tile < 0) break;
       const int g = tile / SPG;
-      const int sl = (tile - g * SPG) * kConsumerWarps + warp;
+      const int sl = (tile - g * SPG) * NSL + warp;
       if (g != cur_g) {
         const int start = rt.grp_start[g], cnt = rt.grp_cnt[g];
         const uint4* h0 =
@@ -610,7 +648,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       }
       if (j == 0 && tid == 0) stamp(a, 14);
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint4* bp = reinterpret_cast<const uint4*>(ring + (size_t)s * dsuper + (size_t)warp * a.d_tile) + lane;
+      const uint4* bp =
+          reinterpret_cast<const uint4*>(ring + (size_t)cell_tab[s * kConsumerWarps + warp] * a.d_tile) + lane;
 #pragma unroll
       for (int q = 0; q < kMaxDownChunks; ++q) {
         if (q < kpd) {

@@ -78,7 +78,6 @@ struct moe_layer {
   int ks = 1;               // hidden-dim split of the router matvec
   int s_gu = 0, s_d = 0;    // gate/up ring depth, down stages
   uint32_t tile_gu = 0, tile_d = 0, ring_bytes = 0;
-  uint32_t d_need[kMaxDownStages] = {};  // gate/up stages (bit 31: reduction area) under each down stage
   size_t smem_max = 0;      // dynamic shared memory at M = MOE_MAX_TOKENS
   LayerKernel kernel = nullptr;
   std::map<int, GraphEntry> graphs;
@@ -133,7 +132,6 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   la.d_tile = h->tile_d;
   la.ring_bytes = h->ring_bytes;
   la.trace = trace ? 1 : 0;
-  for (int d = 0; d < kMaxDownStages; ++d) la.d_need[d] = h->d_need[d];
   la.ws = h->ws;
 
   cudaLaunchAttribute attr[1];
@@ -195,6 +193,11 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
     set_err("inter = %d unsupported: need one of {128, 256, 512}", inter);
     return nullptr;
   }
+  if (hidden % inter != 0) {
+    set_err("hidden = %d is not a multiple of inter = %d (a gate/up tile must be whole down slabs)",
+            hidden, inter);
+    return nullptr;
+  }
   if (topk < 1 || topk > kMaxTopk) { set_err("topk = %d outside [1, %d]", topk, kMaxTopk); return nullptr; }
   if (n_experts < topk || n_experts > kMaxExperts) {
     set_err("n_experts = %d outside [topk, %d]", n_experts, kMaxExperts);
@@ -242,22 +245,15 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   const size_t avail = optin > fixed ? optin - fixed : 0;
   const size_t red = layer_reduction_bytes();
   h->s_gu = avail > red ? (int)std::min<size_t>(kMaxGateUpStages, (avail - red) / h->tile_gu) : 0;
-  const size_t d_stage = (size_t)kConsumerWarps * h->tile_d;  // one slab per consumer warp
-  h->s_d = (int)std::min<size_t>(kMaxDownStages, avail / d_stage);
+  // The down phase reuses the ring as slab-sized cells (a gate/up tile is
+  // hidden/inter whole slabs of 8 rows x I); a down slot is 8 cells, one
+  // slab per consumer warp.
+  h->ring_bytes = (uint32_t)((size_t)h->s_gu * h->tile_gu + red);
+  h->s_d = (int)std::min<size_t>(kMaxDownStages, h->ring_bytes / ((size_t)kConsumerWarps * h->tile_d));
   if (h->s_gu < 2 || h->s_d < 2) {
     set_err("not enough shared memory for the staging rings");
     free_layer(h);
     return nullptr;
-  }
-  h->ring_bytes = (uint32_t)std::max<size_t>((size_t)h->s_gu * h->tile_gu + red, (size_t)h->s_d * d_stage);
-  // which earlier occupants of the ring bytes each down stage must wait for
-  for (int d = 0; d < h->s_d; ++d) {
-    const size_t lo = (size_t)d * d_stage, hi = lo + d_stage;
-    uint32_t need = 0;
-    for (int st = 0; st < h->s_gu; ++st)
-      if (lo < (size_t)(st + 1) * h->tile_gu && (size_t)st * h->tile_gu < hi) need |= 1u << st;
-    if (hi > (size_t)h->s_gu * h->tile_gu) need |= 1u << 31;  // reduction area (or beyond)
-    h->d_need[d] = need;
   }
   h->smem_max = layer_smem_bytes(h->ring_bytes, np_max, n_experts);
 
@@ -462,7 +458,7 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
   o->gateup_stages = h->s_gu;
   o->down_stages = h->s_d;
   o->gateup_tile_bytes = (int)h->tile_gu;
-  o->down_tile_bytes = (int)h->tile_d;
+  o->down_tile_bytes = (int)(h->tile_d * kConsumerWarps);
   o->weight_bytes = h->weight_bytes;
   o->workspace_bytes = h->ws_bytes;
   o->kernels_per_forward = 1;
