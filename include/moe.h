@@ -214,7 +214,8 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
  *         %globaltimer values in ns: 0 dependency wait passed, 1 router
  *         matvec done, 2 grid barrier passed, 3 top-k + compaction done,
  *         4 first gate/up tile consumed, 5 gate/up loop left, 6 every CTA's
- *         SwiGLU rows written, 7 down loop left, 8 combine done, 9 producer
+ *         SwiGLU rows written, 7 down loop left, 8 combine done (the
+ *         CTAs that combine), 9 producer
  *         issued its last gate/up tile, 10 producer issued its last
  *         down tile, 12 top-k done, 13 compaction done, 14 first down
  *         tile consumed, 15 slab arrivals complete; slot 11 holds the

@@ -23,7 +23,8 @@ constexpr int kDownTileRows = 8;      // 8 output rows (n8) x I per down tile
 constexpr int kMaxGateUpStages = 7;   // < 8 reduction slots: see the reduction-slot argument
 constexpr int kMaxDownStages = 8;     // down slots (ring regions of one 8-slab super tile)
 constexpr int kMaxDownChunks = 16;    // 32-wide k chunks of a down row: I <= 512
-constexpr uint32_t kBulkChunk = 16384;  // bytes per cp.async.bulk
+constexpr uint32_t kBulkChunk = 65536;  // bytes per cp.async.bulk (fewer, larger copies: each
+                                        // issue costs the producer shared-memory pipe slots)
 constexpr int kTraceSlots = 32;       // per-CTA phase timestamps of a traced call
 
 // Grid-wide synchronisation words (unsigned, 128 bytes apart).  The 64-bit

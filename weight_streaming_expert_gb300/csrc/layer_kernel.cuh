@@ -87,7 +87,7 @@ constexpr uint32_t kOffCells = 608;   // [8][8] int: ring cell of (down slot, co
 constexpr uint32_t kRingOff = 896;
 constexpr int kRedSlots = 8;
 constexpr uint32_t kRedBytes = kRedSlots * kConsumerWarps * 32 * 16;
-constexpr int kStaticNum = 3, kStaticDen = 4;  // statically split share of the groups
+constexpr int kStaticNum = 7, kStaticDen = 8;  // statically split share of the groups
 static_assert(kMaxGateUpStages <= 8 && kMaxDownStages <= 8, "barrier map");
 static_assert(kOffCall + 8 <= kOffTile && kOffTile + 4 * kMaxGateUpStages <= kOffDTile &&
                   kOffDReady + 8 * kMaxDownStages <= kOffCells &&
@@ -452,6 +452,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       return true;
     };
     int dyn_d = n_s2 <= 1 ? Ts2 + (int)atomicAdd(next_d, 1u) : 0;
+    int cur_dg = -1, cur_de = 0;
     int j2 = 0;
     for (; ok; ++j2) {
       int tile;
@@ -477,16 +478,33 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       // the copy first (weights never depend on h), then the id once the
       // group's h rows are ready
       const int g = tile / SPG, q = tile - g * SPG;
+      if (g != cur_dg) {  // the group's expert (smem reads compete with the consumers')
+        cur_dg = g;
+        cur_de = rt.grp_expert[g];
+      }
       mbar_arrive_expect_tx(dfull(s), dsuper);
-      {  // the 8 slabs are contiguous in global memory; one copy per run of adjacent cells
-        const uint8_t* src = a.w_down + ((size_t)rt.grp_expert[g] * SL + (size_t)q * NSL) * a.d_tile;
-        const int* cells = cell_tab + s * kConsumerWarps;
-        int w0 = 0;
-        for (int w = 1; w <= NSL; ++w) {
-          if (w < NSL && cells[w] == cells[w - 1] + 1) continue;
-          bulk_g2s_chunked(ring_u32 + (uint32_t)cells[w0] * a.d_tile, src + (size_t)w0 * a.d_tile,
-                           (uint32_t)(w - w0) * a.d_tile, dfull(s));
-          w0 = w;
+      {  // the 8 slabs are contiguous in global memory; one copy per run of
+         // adjacent cells, the runs worked out arithmetically (list positions
+         // 8s .. 8s + 7, stage boundaries every cps positions)
+        const uint8_t* src = a.w_down + ((size_t)cur_de * SL + (size_t)q * NSL) * a.d_tile;
+        int p = s * kConsumerWarps, left = NSL, w0 = 0;
+        int r = p / cps, within = p - r * cps;
+        while (left > 0) {
+          int run, cell;
+          if (p >= gu_cells) {
+            run = left;
+            cell = p;
+          } else {
+            run = min(left, cps - within);
+            cell = ((n_gu + r) % S) * cps + within;
+          }
+          bulk_g2s_chunked(ring_u32 + (uint32_t)cell * a.d_tile, src + (size_t)w0 * a.d_tile,
+                           (uint32_t)run * a.d_tile, dfull(s));
+          p += run;
+          w0 += run;
+          left -= run;
+          ++r;
+          within = 0;
         }
       }
       if (!ensure_ready(g)) {
@@ -672,21 +690,28 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     if (tid == 0) stamp(a, 7);
   }
 
-  // ---- 6. every CTA's weighted rows written -> combine.  CTA c owns the
-  // 8-row output slabs c, c + grid, ...: each token's k rows summed in slot
-  // order, ONE bf16 rounding.
+  // ---- 6. every CTA's weighted rows written -> combine.  Only the first
+  // n_own_ctas CTAs combine (8 output slabs each: CTA c owns 8c .. 8c+7):
+  // each token's k rows summed in slot order, ONE bf16 rounding.  The other
+  // CTAs count themselves in and leave at once, so the next call's CTAs get
+  // their SMs (and run their prologue) while the combine runs.
+  const int n_own_ctas = min((int)gridDim.x, (SL + kConsumerWarps - 1) / kConsumerWarps);
+  const int own_per = (SL + n_own_ctas - 1) / n_own_ctas;  // 8 unless the grid is small
+  const bool owner = (int)blockIdx.x < n_own_ctas;
   consumers_sync();
   if (tid == 0) {
     grid_count(a.ws.sync + kSyncCount);
-    grid_wait(a.ws, a.ws.sync + kSyncCount, 2ull * *call_idx * gridDim.x, 3);
+    if (owner) grid_wait(a.ws, a.ws.sync + kSyncCount, 2ull * *call_idx * gridDim.x, 3);
   }
+  if (!owner) return;
   consumers_sync();
   if (tid == 0) stamp(a, 15);
   const int nthr = kConsumerWarps * 32;
-  const int n_own = SL > (int)blockIdx.x ? (SL - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int sl0 = (int)blockIdx.x * own_per;
+  const int n_own = max(0, min(own_per, SL - sl0));
   const int per = a.M * kDownTileRows;
   for (int it = tid; it < n_own * per; it += nthr) {
-    const int sl = (int)blockIdx.x + (it / per) * (int)gridDim.x;
+    const int sl = sl0 + it / per;
     const int m = (it % per) / kDownTileRows;
     const int r = sl * kDownTileRows + (it % kDownTileRows);
     const float* yr = a.ws.y + (size_t)m * a.K * a.H + r;
