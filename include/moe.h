@@ -210,18 +210,21 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
 /*
  * moe_read_trace -- copy the phase timestamps of the last call made with
  * MOE_FWD_TRACE (synchronises the device; profiling aid).
- *   out   host uint64 [cap]: for CTA c, slots [16c, 16c + 16) hold
+ *   out   host uint64 [cap]: for CTA c, slots [32c, 32c + 32) hold
  *         %globaltimer values in ns: 0 dependency wait passed, 1 router
  *         matvec done, 2 grid barrier passed, 3 top-k + compaction done,
  *         4 first gate/up tile consumed, 5 gate/up loop left, 6 every CTA's
- *         SwiGLU rows written, 7 down loop left, 8 combine done (the
- *         CTAs that combine), 9 producer
- *         issued its last gate/up tile, 10 producer issued its last
- *         down tile, 12 top-k done, 13 compaction done, 14 first down
- *         tile consumed, 15 slab arrivals complete; slot 11 holds the
- *         CTA's gate/up tile COUNT.  Slots of phases a CTA did not reach
- *         keep older values.
- * Returns the number of values written (min(cap, 16 x SMs)), or on error
+ *         statically split gate/up tiles reduced (publisher), 7 down loop
+ *         left, 8 combine done (the CTAs that combine), 9 producer issued
+ *         its last gate/up tile, 10 producer issued its last down tile,
+ *         12 top-k done, 13 compaction done, 14 first down tile consumed,
+ *         15 weighted rows of every CTA written (combining CTAs), 17 every
+ *         CTA's gate/up tiles reduced (publisher), 18 this CTA's static
+ *         gate/up tiles counted in, 19 CTA started, 20 prologue done (before
+ *         the dependency wait).  Slot 11 holds the CTA's gate/up tile COUNT
+ *         and slot 16 its down super-tile COUNT.  Slots of phases a CTA did
+ *         not reach keep older values.
+ * Returns the number of values written (min(cap, 32 x SMs)), or on error
  * the negated moe_status_t (a positive status could not be told apart from a
  * count).
  */

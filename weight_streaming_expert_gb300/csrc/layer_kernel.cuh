@@ -29,10 +29,12 @@
 //  3. EVERY CTA computes the top-k of all tokens and the compaction itself
 //     (shared memory only): nothing is published and re-read, no second
 //     launch, no last-CTA hand-off.  The results are bitwise equal in all
-//     CTAs (same inputs, same code), so they agree on every position.
+//     CTAs (same inputs, same code), so they agree on every position.  With
+//     at most 16 tokens every chosen expert is one group and the compaction
+//     is worked out on the pair axis (two short loops, no scan).
 //  4. Gate/up: (group, 8-row) tiles of 8 weight rows x H, staged by the
 //     producer with bulk copies into a ring of mbarrier-guarded stages.
-//     The tiles of the first 3/4 of the groups are split statically, the
+//     The tiles of the first 7/8 of the groups are split statically, the
 //     rest are taken one at a time from a global counter, so SMs that stream
 //     faster take more (the per-SM rate differs by several per cent).  The producer writes each
 //     stage's tile id and signals it before the copy lands, so consumers
@@ -40,7 +42,7 @@
 //     reducer warp sums their partials in a fixed order and applies SwiGLU.
 //  5. Down: (group, 64-output-row) super tiles = 8 slabs of 8 rows x I,
 //     one slab per consumer warp, staged the same way (the same producer,
-//     the same 3/4 static + dynamic tail split, the same early tile ids).
+//     the same 7/8 static + dynamic tail split, the same early tile ids).
 //     The producer puts the first down super tiles into ring bytes as soon
 //     as the gate/up tiles there are consumed for the last time -- HBM does
 //     not drain between the two GEMVs.  No grid-wide barrier sits between
@@ -274,8 +276,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   }
   __syncthreads();
   if (tid == 0) stamp(a, 12);
-  compact_masks(rt, a.M, a.K, a.E);
-  const int n_groups = rt.scal[0];
+  // the reduction area is free until the gate/up loop: scratch for the
+  // pair-axis compaction
+  const int n_groups = a.M <= kGroupTokens
+                           ? compact_pairs(rt, NP, a.K, reinterpret_cast<int*>(red), tid, kExpertThreads)
+                           : (compact_masks(rt, a.M, a.K, a.E), rt.scal[0]);
   if (tid == 0) stamp(a, 13);
   if (blockIdx.x == 0) {  // a copy for inspection (moe_read_routing); nothing reads it back
     for (int i = tid; i < NP; i += kExpertThreads) {

@@ -25,12 +25,15 @@
 //    product unchanged).  Units write fp32 partial logits; the reader sums
 //    the ks partials in a fixed order, so the logits are deterministic.
 //  * Top-k, one warp per token: the E logits sit in registers (lane l holds
-//    experts l + 32v as order-preserving integer keys); k rounds of a
-//    redux.sync arg-max (largest key; ties -- bit-equal logits -- to the
-//    lowest expert id), after which every lane re-reduces its own keys with
-//    a depth-log2 tree (branch-free).  Weights: exp(l_j - l_0) over the k
-//    chosen, normalised by their sum (= the full softmax renormalised over
-//    the k; its denominator cancels).
+//    experts l + 32v as order-preserving integer keys).  Every lane first
+//    lists its two best keys (a max/min tree, then the lowest positions
+//    holding them).  A round takes the warp's best list head (redux.sync max
+//    of the keys, then redux.sync min of the expert ids holding it: ties --
+//    bit-equal logits -- go to the lowest id) and the winning lane shifts
+//    its list; a lane that gives both of its keys refills the list with the
+//    next two below the last one (rare: it holds three of the winners).
+//    Weights: exp(l_j - l_0) over the k chosen, normalised by their sum
+//    (= the full softmax renormalised over the k; its denominator cancels).
 //  * Compaction from bit masks: an expert is chosen at most once per token,
 //    so bit m of mask[e] says "token m chose e".  popc(mask[e]) is the
 //    bucket size and popc(mask[e] & (2^m - 1)) the pair's stable rank in its
@@ -144,42 +147,60 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Arg-max of key[0..VPL) by a tree (ties keep the lower index).
+// The two best keys of key[0..VPL) strictly below (lk, lv) in the order
+// (key desc, position asc), with the lowest positions holding them; a
+// missing entry is (0, VPL).  A max/min tree finds the keys (no
+// predicates: the dependent chain is short), match masks their positions.
 template <int VPL>
-__device__ __forceinline__ void tree_argmax(const uint32_t (&key)[VPL], uint32_t& best, int& bv) {
-  uint32_t tk[VPL];
-  int tv[VPL];
+__device__ __forceinline__ void top2_below(const uint32_t (&key)[VPL], uint32_t lk, int lv, uint32_t& k1,
+                                           int& v1, uint32_t& k2, int& v2) {
+  uint32_t kf[VPL];
 #pragma unroll
-  for (int v = 0; v < VPL; ++v) {
-    tk[v] = key[v];
-    tv[v] = v;
-  }
+  for (int v = 0; v < VPL; ++v) kf[v] = (key[v] < lk || (key[v] == lk && v > lv)) ? key[v] : 0u;
+  uint32_t hi[VPL > 1 ? VPL / 2 : 1], lo[VPL > 1 ? VPL / 2 : 1];
+  if constexpr (VPL == 1) {
+    hi[0] = kf[0];
+    lo[0] = 0u;
+  } else {
 #pragma unroll
-  for (int s = 1; s < VPL; s <<= 1) {
+    for (int i = 0; i < VPL / 2; ++i) {
+      hi[i] = max(kf[2 * i], kf[2 * i + 1]);
+      lo[i] = min(kf[2 * i], kf[2 * i + 1]);
+    }
+    // merging two (best, second) pairs: best of the bests; second = the
+    // better of the losing best and the two seconds
 #pragma unroll
-    for (int v = 0; v + s < VPL; v += 2 * s) {
-      if (tk[v + s] > tk[v]) {
-        tk[v] = tk[v + s];
-        tv[v] = tv[v + s];
+    for (int s = 1; s < VPL / 2; s <<= 1) {
+#pragma unroll
+      for (int i = 0; i + s < VPL / 2; i += 2 * s) {
+        const uint32_t h = max(hi[i], hi[i + s]);
+        lo[i] = max(min(hi[i], hi[i + s]), max(lo[i], lo[i + s]));
+        hi[i] = h;
       }
     }
   }
-  best = tk[0];
-  bv = tv[0];
+  k1 = hi[0];
+  k2 = lo[0];
+  uint32_t m1 = 0u, m2 = 0u;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    m1 |= (kf[v] == k1 ? 1u : 0u) << v;
+    m2 |= (kf[v] == k2 ? 1u : 0u) << v;
+  }
+  v1 = __ffs(m1) - 1;
+  if (k2 == k1) m2 &= m2 - 1u;  // the same key twice: its second position
+  v2 = k2 == 0u ? VPL : __ffs(m2) - 1;
 }
 
 // Top-k of one token by one warp.  lg: the token's partial logits (plane 0;
 // ks planes `plane` floats apart), summed in plane order, plus the bias.
 // Lane j < K writes slot j's expert id to idx_out[j] (the caller reads them
 // after a __syncwarp) and returns slot j's renormalised weight; the other
-// lanes return 0.  A round: redux.sync max of the lane bests, redux.sync min
-// of the ids holding it (ties -- bit-equal logits -- to the lowest id; inside
-// a lane the tree keeps the lower index, i.e. the lower id), then every lane
-// drops the winner if it holds it and re-reduces with the tree.
+// lanes return 0.
 template <int VPL>
-__device__ float topk_token(const float* __restrict__ lg, size_t plane, int ks,
-                            const float* __restrict__ bias, int E, int K, int lane, int* status,
-                            int* idx_out) {
+__device__ __forceinline__ float topk_token(const float* __restrict__ lg, size_t plane, int ks,
+                                            const float* __restrict__ bias, int E, int K, int lane,
+                                            int* status, int* idx_out) {
   // planes 0 and 1 and the bias in one round trip; further planes one each;
   // the sum order is plane 0, 1, ..., then the bias
   float lv[VPL], l1[VPL], bv_[VPL];
@@ -211,39 +232,40 @@ __device__ float topk_token(const float* __restrict__ lg, size_t plane, int ks,
     if (bias) lv[v] += bv_[v];
     key[v] = e < E ? ordered_key(lv[v]) : 0u;
   }
-  uint32_t best;
-  int bv;
-  tree_argmax<VPL>(key, best, bv);
+  uint32_t k1, k2;
+  int v1, v2;
+  top2_below<VPL>(key, 0xffffffffu, -1, k1, v1, k2, v2);
 
-  // branch-free rounds: a divergent winner-only update costs more than the
-  // second redux and the all-lane rescan it would save
-  uint32_t my_key = 0u;
+  uint32_t my_key = 0u, my_win = 0u, top0 = 0u;
   for (int j = 0; j < K; ++j) {
-    const uint32_t top = __reduce_max_sync(0xffffffffu, best);
-    const uint32_t cand = (best == top) ? (uint32_t)(bv * 32 + lane) : 0xffffffffu;
-    uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-    if (top == 0u || win >= (uint32_t)E) {  // unreachable while K <= E
-      if (lane == 0) set_error(status, kErrBadIndex);
-      win = 0;
-    }
-    if (lane == j) {
-      my_key = top;
-      idx_out[j] = (int)win;
-    }
+    const uint32_t top = __reduce_max_sync(0xffffffffu, k1);
+    const uint32_t cand = (k1 == top) ? (uint32_t)(v1 * 32 + lane) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    top0 = j == 0 ? top : top0;
+    my_key = lane == j ? top : my_key;
+    my_win = lane == j ? win : my_win;
     const bool mine = (int)(win & 31u) == lane;
-    const int wv = (int)(win >> 5);
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) key[v] = (mine && v == wv) ? 0u : key[v];
-    tree_argmax<VPL>(key, best, bv);
+    const uint32_t gk = k1;
+    const int gv = v1;
+    k1 = mine ? k2 : k1;
+    v1 = mine ? v2 : v1;
+    k2 = mine ? 0u : k2;
+    v2 = mine ? VPL : v2;
+    if (mine && v1 >= VPL && j + 1 < K) top2_below<VPL>(key, gk, gv, k1, v1, k2, v2);
   }
-  // weights: exp(l_j - l_0), normalised by a fixed butterfly sum
-  const float my_val = key_value(my_key);
-  const float v0 = __shfl_sync(0xffffffffu, my_val, 0);
-  const float ex = lane < K ? expf(my_val - v0) : 0.f;
+  if (lane < K) {
+    if (my_key == 0u || my_win >= (uint32_t)E) {  // unreachable while K <= E
+      set_error(status, kErrBadIndex);
+      my_win = 0u;
+    }
+    idx_out[lane] = (int)my_win;
+  }
+  // weights: exp(l_j - l_0), normalised by a fixed butterfly sum over the
+  // lanes that hold one (lanes >= K add 0)
+  const float ex = lane < K ? expf(key_value(my_key) - key_value(top0)) : 0.f;
   float s = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return lane < K ? ex / s : 0.f;
+  for (int o = 1; o < K; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return lane < K ? __fdividef(ex, s) : 0.f;
 }
 
 __device__ __forceinline__ float topk_dispatch(const float* lg, size_t plane, int ks, const float* bias,
@@ -370,6 +392,48 @@ __device__ inline void compact_masks(const SmemRouting& r, int M, int K, int E) 
     r.pair_list[r.s_off[e] + rank] = p;
   }
   __syncthreads();
+}
+
+// M <= kGroupTokens: every expert's bucket holds at most M <= 16 pairs, so
+// it is exactly one group, and the groups are the chosen experts in
+// ascending id (the same result as compact_masks).  Worked out on the pair
+// axis ("Two fusions and a retune": moe_align compares pairs instead of
+// scanning experts): pair p with expert e goes to
+//   position = #{q : e_q < e} + #{q < p : e_q = e},
+// and the pair of e with the lowest token opens e's group, numbered by the
+// group openers with a smaller expert.  Two short loops over the NP pairs
+// per thread (the code stays small: it runs once per call, cold), no scan.
+// ekey: NP ints of scratch.  Cooperative over threads t, t + nt, ...; mask[]
+// and s_e[] complete and visible (a barrier before); scal[0] zero.  Ends
+// with a __syncthreads(); returns the group count.
+__device__ inline int compact_pairs(const SmemRouting& r, int NP, int K, int* ekey, int t, int nt) {
+  for (int p = t; p < NP; p += nt) {
+    const int e = r.s_e[p], m = p / K;
+    ekey[p] = (e << 1) | ((r.mask[e] & ((1ull << m) - 1ull)) == 0ull ? 1 : 0);
+  }
+  __syncthreads();
+  for (int p = t; p < NP; p += nt) {
+    const int ek = ekey[p], e = ek >> 1;
+    int below = 0, open_below = 0, same_before = 0;
+    for (int q = 0; q < NP; ++q) {
+      const int f = ekey[q];
+      const int lt = (f >> 1) < e ? 1 : 0;
+      below += lt;
+      open_below += lt & f;
+      same_before += ((f >> 1) == e && q < p) ? 1 : 0;
+    }
+    r.pair_list[below + same_before] = p;
+    if (ek & 1) {
+      r.grp_expert[open_below] = e;
+      r.grp_start[open_below] = below;
+      r.grp_cnt[open_below] = __popcll(r.mask[e]);
+      atomicAdd(&r.scal[0], 1);
+    }
+  }
+  __syncthreads();
+  const int n_groups = r.scal[0];
+  if (t == 0) r.scal[1] = n_groups;
+  return n_groups;
 }
 
 }  // namespace wse
