@@ -158,18 +158,28 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // Bulk (TMA) copy global -> shared, completion counted in bytes on `bar`.
 // dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
+// L2 policy for data read once per call (the expert weights): evict it
+// first, so that what every call re-reads -- the kernel's code, the tokens,
+// the router weights, the partial logits, h and y -- stays in L2 while
+// hundreds of MB of weights stream past.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void bulk_g2s_chunked(uint32_t dst, const uint8_t* src, uint32_t bytes,
-                                                 uint32_t bar) {
+                                                 uint32_t bar, uint64_t policy) {
   for (uint32_t off = 0; off < bytes; off += kBulkChunk) {
     uint32_t n = bytes - off < kBulkChunk ? bytes - off : kBulkChunk;
-    bulk_g2s(dst + off, src + off, n, bar);
+    bulk_g2s(dst + off, src + off, n, bar, policy);
   }
 }
 

@@ -362,6 +362,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int q0 = (int)((long long)Ts2 * blockIdx.x / gridDim.x);
     const int q1 = (int)((long long)Ts2 * (blockIdx.x + 1) / gridDim.x);
     unsigned* next_gu = a.ws.sync + kSyncGateUpNext;
+    const uint64_t wpol = l2_evict_first_policy();  // expert weights: read once per call
     unsigned* next_d = a.ws.sync + kSyncDownNext;
     // tiles of the shared tails are taken one ahead (the atomic's round trip
     // hides behind a tile), starting one tile before the static share ends:
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       const int g = tile / TPG, tt = tile - g * TPG;
       mbar_arrive_expect_tx(full(s), a.gu_tile);
       bulk_g2s_chunked(ring_u32 + (uint32_t)s * a.gu_tile,
-                       a.w_gate_up + ((size_t)rt.grp_expert[g] * TPG + tt) * a.gu_tile, a.gu_tile, full(s));
+                       a.w_gate_up + ((size_t)rt.grp_expert[g] * TPG + tt) * a.gu_tile, a.gu_tile, full(s), wpol);
     }
     const int n_gu = j;
     if (ok) {  // end marker for the consumers
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
             cell = ((n_gu + r) % S) * cps + within;
           }
           bulk_g2s_chunked(ring_u32 + (uint32_t)cell * a.d_tile, src + (size_t)w0 * a.d_tile,
-                           (uint32_t)run * a.d_tile, dfull(s));
+                           (uint32_t)run * a.d_tile, dfull(s), wpol);
           p += run;
           w0 += run;
           left -= run;
