@@ -364,9 +364,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     unsigned* next_gu = a.ws.sync + kSyncGateUpNext;
     const uint64_t wpol = l2_evict_first_policy();  // expert weights: read once per call
     unsigned* next_d = a.ws.sync + kSyncDownNext;
-    // tiles of the shared tails are taken one ahead (the atomic's round trip
-    // hides behind a tile), starting one tile before the static share ends:
-    // a tile taken earlier would be held back from faster SMs
+    // gate/up tiles of the shared tail are taken one ahead (the atomic's
+    // round trip hides behind a tile), starting one tile before the static
+    // share ends: a tile taken earlier would be held back from faster SMs.
+    // Down tiles of the shared tail are taken only once a slot is free (the
+    // slots in flight hide the round trip), so that at the end no CTA holds
+    // a tile it cannot start while others have none.
     const int n_s = s1 - s0, n_s2 = q1 - q0;
     int dyn_gu = n_s <= 1 ? Ts + (int)atomicAdd(next_gu, 1u) : 0;
     bool ok = true;
@@ -457,19 +460,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       }
       return true;
     };
-    int dyn_d = n_s2 <= 1 ? Ts2 + (int)atomicAdd(next_d, 1u) : 0;
-    int cur_dg = -1, cur_de = 0;
     int j2 = 0;
+    int cur_dg = -1, cur_de = 0;
     for (; ok; ++j2) {
-      int tile;
-      if (j2 < n_s2) {
-        tile = q0 + j2;
-        if (j2 == n_s2 - 2) dyn_d = Ts2 + (int)atomicAdd(next_d, 1u);
-      } else {
-        tile = dyn_d;
-        if (tile < T_d) dyn_d = Ts2 + (int)atomicAdd(next_d, 1u);
-      }
-      if (tile >= T_d) break;
       const int s = j2 % SD;
       if (j2 < SD) {
         if (!release_until(slot_rank(s))) {
@@ -481,6 +474,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         ok = false;
         break;
       }
+      const int tile = j2 < n_s2 ? q0 + j2 : Ts2 + (int)atomicAdd(next_d, 1u);
+      if (tile >= T_d) break;
       // the copy first (weights never depend on h), then the id once the
       // group's h rows are ready
       const int g = tile / SPG, q = tile - g * SPG;
