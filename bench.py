@@ -431,7 +431,9 @@ def run_ours(args):
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
         if tr.get("source_hash") == source_hash(LAYER_SOURCES) and tr.get("M") == M:
-            traffic = tr.get("bytes_per_launch")
+            # measured on a smaller run (one layer, 8 calls): DRAM traffic
+            # follows the algorithmic bytes, so scale it to this run's launches
+            traffic = int(round(tr["bytes_per_launch"] * bytes_call / tr["algorithmic_bytes_per_launch"]))
     e2e_us, h2d, d2h = (None, 0, 0)
     if not args.no_e2e:
         e2e_us, h2d, d2h = time_e2e(wkl, min(args.steps, 4000))

@@ -49,6 +49,18 @@ def test_call_bytes_count_router_and_io_once():
     assert bench.algorithmic_bytes(2560, 512, 8, 512, M=6, n_active=46) - base == 46 * 3 * 2560 * 512 * 2
 
 
+def test_traffic_record_is_complete_and_near_the_algorithmic_bytes():
+    # the committed ncu record the bench scales into roofline.traffic
+    with open(bench.TRAFFIC_FILE) as f:
+        tr = json.load(f)
+    for key in ("source_hash", "M", "bytes_per_launch", "algorithmic_bytes_per_launch", "launches", "command"):
+        assert key in tr
+    reads = [l["dram_read"] + l["dram_write"] for l in tr["launches"]]
+    assert abs(sum(reads) / len(reads) - tr["bytes_per_launch"]) <= 1e-6 * tr["bytes_per_launch"] + 1
+    # DRAM traffic of a cold call is its algorithmic bytes, give or take a few per cent
+    assert 0.97 <= tr["bytes_per_launch"] / tr["algorithmic_bytes_per_launch"] <= 1.05
+
+
 def test_layer_count_keeps_l2_cold():
     from weight_streaming_expert_gb300 import workloads as wl
     l2 = 126 * 1024 * 1024
