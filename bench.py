@@ -14,6 +14,7 @@ and replayed; CUDA events on the launching stream bracket exactly K calls,
 with a barrier and a device synchronize on both sides; max over ranks.
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--M 6] [--zipf]
+    python bench.py --shape ling_tp4      # the per-GPU slice of a 4-way TP split (inter 128)
     python bench.py --impl reference     # the CPU oracle on the same workload
     python bench.py --sweep               # M x routing sweep (writes JSON lines)
 """
@@ -412,7 +413,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     prop = torch.cuda.get_device_properties(dev)
     l2 = getattr(prop, "L2_cache_size", L2_BYTES) or L2_BYTES
-    shape = wl.LING
+    shape = wl.SHAPES[args.shape]
     M = args.M
     n_layers = n_layers_for(M, shape, l2, args.layers)
     wkl = Workload(shape, n_layers, M, args.pool, args.zipf, dev)
@@ -430,7 +431,8 @@ def run_ours(args):
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
-        if tr.get("source_hash") == source_hash(LAYER_SOURCES) and tr.get("M") == M:
+        if (tr.get("source_hash") == source_hash(LAYER_SOURCES) and tr.get("M") == M
+                and args.shape == tr.get("shape", "ling")):
             # measured on a smaller run (one layer, 8 calls): DRAM traffic
             # follows the algorithmic bytes, so scale it to this run's launches
             traffic = int(round(tr["bytes_per_launch"] * bytes_call / tr["algorithmic_bytes_per_launch"]))
@@ -466,8 +468,10 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens (random init, no checkpoint)",
-            "config": {"workload": f"Ling-shaped MoE {'block-verify' if M >= 16 else 'verify' if M > 1 else 'decode'} step: "
-                                   f"hidden 2560, 512 experts, top-8 softmax+renorm, SwiGLU inter 512, "
+            "config": {"workload": f"Ling-shaped MoE {'block-verify' if M >= 16 else 'verify' if M > 1 else 'decode'} step"
+                                   f"{' (per-GPU slice of a 4-way TP split)' if args.shape == 'ling_tp4' else ''}: "
+                                   f"hidden {shape.hidden}, {shape.n_experts} experts, top-{shape.topk} softmax+renorm, "
+                                   f"SwiGLU inter {shape.inter}, "
                                    f"M={M}, {'Zipf(1.1) router bias' if args.zipf else 'uniform routing'}",
                        "M": M, "layers_cycled": n_layers, "x_pool": args.pool,
                        "l2_policy": f"inputs larger than L2: {n_layers} distinct layer weight sets cycled, "
@@ -502,7 +506,7 @@ def run_reference(args):
     if rank != 0:
         return
     from weight_streaming_expert_gb300 import workloads as wl
-    shape = wl.LING
+    shape = wl.SHAPES[args.shape]
     budget = args.cpu_budget
     # warmup samples (untimed), then timed samples bounded by the budget
     us_w, _, host = oracle_call_us(shape, args.M, args.zipf, budget_s=0.0,
@@ -515,7 +519,8 @@ def run_reference(args):
         "steps": n, "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate over bf16",
         "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens",
-        "config": {"workload": f"Ling-shaped MoE step: hidden 2560, 512 experts, top-8, inter 512, M={args.M}",
+        "config": {"workload": f"Ling-shaped MoE step: hidden {shape.hidden}, {shape.n_experts} experts, "
+                               f"top-{shape.topk}, inter {shape.inter}, M={args.M}",
                    "M": args.M},
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{n} single-token oracle calls (of {args.steps} requested steps, "
@@ -530,7 +535,7 @@ def run_sweep(args):
     from weight_streaming_expert_gb300 import workloads as wl
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    shape = wl.LING
+    shape = wl.SHAPES[args.shape]
     peak, peak_kind = measured_peaks()
     wkl = Workload(shape, args.layers or 8, 1, args.pool, False, dev)
     for zipf in (False, True):
@@ -555,6 +560,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--M", type=int, default=6)
+    ap.add_argument("--shape", choices=["ling", "ling_tp4"], default="ling",
+                    help="ling: hidden 2560, 512 experts, top-8, inter 512; ling_tp4: its 4-way TP slice, inter 128")
     ap.add_argument("--zipf", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets (0 = auto)")
     ap.add_argument("--pool", type=int, default=64, help="distinct token batches cycled")

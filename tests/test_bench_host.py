@@ -53,7 +53,7 @@ def test_traffic_record_is_complete_and_near_the_algorithmic_bytes():
     # the committed ncu record the bench scales into roofline.traffic
     with open(bench.TRAFFIC_FILE) as f:
         tr = json.load(f)
-    for key in ("source_hash", "M", "bytes_per_launch", "algorithmic_bytes_per_launch", "launches", "command"):
+    for key in ("source_hash", "shape", "M", "bytes_per_launch", "algorithmic_bytes_per_launch", "launches", "command"):
         assert key in tr
     reads = [l["dram_read"] + l["dram_write"] for l in tr["launches"]]
     assert abs(sum(reads) / len(reads) - tr["bytes_per_launch"]) <= 1e-6 * tr["bytes_per_launch"] + 1

@@ -171,6 +171,27 @@ def test_ling_sweep(oracle, ling, M, zipf):
     run_and_check(oracle, layer, host, x, wl.LING.topk, bias=bias)
 
 
+@pytest.fixture(scope="module")
+def ling_tp4(MoELayer):
+    """The per-GPU slice of a 4-way TP split of the Ling-shaped layer (inter
+    512 / 4 = 128 rows of every expert), full size, seed 1100."""
+    w_r, w_gu, w_d = wl.layer_weights(wl.LING_TP4, seed=1100, device=DEV)
+    layer = MoELayer(w_r, w_gu, w_d, topk=wl.LING_TP4.topk)
+    host = dict(wr=bits(w_r), wgu=bits(w_gu), wd=bits(w_d))
+    del w_r, w_gu, w_d
+    torch.cuda.empty_cache()
+    yield layer, host
+    layer.close()
+
+
+@pytest.mark.parametrize("M,seed,zipf", [(6, 11, False), (1, 12, False), (16, 13, True), (64, 14, False)])
+def test_ling_tp4_slice(oracle, ling_tp4, M, seed, zipf):
+    layer, host = ling_tp4
+    bias = wl.zipf_router_bias(wl.LING_TP4.n_experts) if zipf else None
+    x = wl.tokens(M, wl.LING_TP4.hidden, seed=3_000_000 + seed, device=DEV)
+    run_and_check(oracle, layer, host, x, wl.LING_TP4.topk, bias=bias)
+
+
 def test_all_tokens_on_the_same_experts(oracle, ling):
     """64 tokens forced onto the same 8 experts: 4 groups of 16 per expert."""
     layer, host = ling

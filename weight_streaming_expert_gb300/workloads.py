@@ -34,6 +34,12 @@ class LayerShape:
 
 TINY = LayerShape(hidden=256, n_experts=16, topk=2, inter=128)
 LING = LayerShape(hidden=2560, n_experts=512, topk=8, inter=512)
+# The per-GPU slice of the post's 4-way tensor-parallel split: every GPU holds
+# inter/4 = 128 rows of every expert's gate/up and the matching 128 columns
+# of its down projection, routes redundantly and streams a quarter of each
+# activated expert (the partial outputs are summed across GPUs afterwards).
+LING_TP4 = LayerShape(hidden=2560, n_experts=512, topk=8, inter=128)
+SHAPES = {"ling": LING, "ling_tp4": LING_TP4}
 
 
 def _gen(seed: int, device) -> torch.Generator:
