@@ -14,7 +14,8 @@
 //   down-GEMM -> combine; the combine as an fp32 sum times a scale with a
 //   single final cast), "Two fusions and a retune" (SwiGLU = silu(gate)*up
 //   evaluated in float with one final rounding; pair-axis bucketing),
-//   "bf16 router gate and lm_head" (router weights in bf16).
+//   "bf16 router gate and lm_head" (router weights in bf16; the vocabulary
+//   projection as a bf16 matrix-vector product, oracle_lm_head).
 //   Layer shape and routing rule (softmax top-k with renormalisation, SwiGLU
 //   experts, bf16 inputs, fp32 accumulation) follow the layer definition the
 //   post's model uses: a 512-expert routed MoE per layer, hidden 2560.
@@ -82,6 +83,23 @@ int oracle_router_logits(int M, int H, int E, const uint16_t* x,
       }
       if (bias) acc = acc + bias[e];
       logits[(size_t)m * E + e] = acc;
+    }
+  }
+  return 0;
+}
+
+// The vocabulary projection of the decode step ("bf16 router gate and
+// lm_head": at batch 1 the lm_head is a bf16 matrix-vector product read once
+// per step): logits[m][v] = sum_k x[m][k] * W[v][k], fp32, ascending k.
+int oracle_lm_head(int M, int H, int V, const uint16_t* x, const uint16_t* w, float* logits) {
+  if (M < 0 || H <= 0 || V <= 0 || !x || !w || !logits) return 1;
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* xr = x + (size_t)m * H;
+    for (int v = 0; v < V; ++v) {
+      const uint16_t* wr = w + (size_t)v * H;
+      float acc = 0.0f;
+      for (int k = 0; k < H; ++k) acc = acc + oracle_bf16_to_f32(xr[k]) * oracle_bf16_to_f32(wr[k]);
+      logits[(size_t)m * V + v] = acc;
     }
   }
   return 0;

@@ -60,8 +60,9 @@ def load(path: str | None = None):
         lib.oracle_expert_down.argtypes = [ci, ci, u16p, u16p, f32p]
         lib.oracle_moe_forward.argtypes = [ci, ci, ci, ci, ci, u16p, u16p, f32p, u16p, u16p,
                                            i32p, f32p, i32p, f32p, f32p, u16p, u16p]
+        lib.oracle_lm_head.argtypes = [ci, ci, ci, u16p, u16p, f32p]
         for name in ("oracle_router_logits", "oracle_topk_softmax", "oracle_weights_for_set",
-                     "oracle_expert_swiglu", "oracle_expert_down", "oracle_moe_forward"):
+                     "oracle_expert_swiglu", "oracle_expert_down", "oracle_moe_forward", "oracle_lm_head"):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
@@ -106,6 +107,18 @@ class Oracle:
         b = None if bias is None else np.ascontiguousarray(bias, np.float32)
         rc = self.lib.oracle_router_logits(M, H, E, _p(x, ctypes.c_uint16), _p(w_router, ctypes.c_uint16),
                                            _p(b, ctypes.c_float), _p(logits, ctypes.c_float))
+        assert rc == 0
+        return logits
+
+    def lm_head(self, x, w):
+        """fp32 logits [M, V] of bf16 tokens x [M, H] and projection w [V, H]."""
+        x, w = _u16(x), _u16(w)
+        M, H = x.shape
+        V = w.shape[0]
+        assert w.shape == (V, H)
+        logits = np.zeros((M, V), np.float32)
+        rc = self.lib.oracle_lm_head(M, H, V, _p(x, ctypes.c_uint16), _p(w, ctypes.c_uint16),
+                                     _p(logits, ctypes.c_float))
         assert rc == 0
         return logits
 

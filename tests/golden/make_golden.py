@@ -1,11 +1,13 @@
-"""Writes tests/golden/tiny_seed0.txt from the CPU oracle.
+"""Writes tests/golden/tiny_seed0.txt and lm_head_seed21.txt from the CPU oracle.
 
 The fixture is a regression record of the oracle on the small oracle-check
 layer (hidden 256, 16 experts, top-2, inter 128, all tensors from seed 0),
 for M = 1 and M = 4.  It lets a run on another host (the GPU machine is an
 Arm host) confirm that the oracle it builds there computes what the pinned
 oracle computed here.  Only the oracle and the seeded input generator are
-called.
+called.  lm_head_seed21.txt does the same for the vocabulary projection
+(hidden 256, a ragged vocabulary of 333 rows from seed 21, two tokens from
+seed 22).
 
     python tests/golden/make_golden.py
 """
@@ -21,6 +23,7 @@ from oracle.oracle import Oracle  # noqa: E402
 from weight_streaming_expert_gb300 import workloads as wl  # noqa: E402
 
 OUT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tiny_seed0.txt")
+OUT_LM = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lm_head_seed21.txt")
 
 
 def main():
@@ -38,6 +41,13 @@ def main():
     with open(OUT, "w") as f:
         f.write("\n".join(lines) + "\n")
     print("wrote", OUT)
+    w = wl.bf16_bits(wl.lm_head_weight(333, 256, seed=21))
+    x = wl.bf16_bits(wl.tokens(2, 256, seed=22))
+    lg = orc.lm_head(x, w)
+    with open(OUT_LM, "w") as f:
+        f.write("# oracle lm_head logits, hidden 256, vocab 333 (seed 21), 2 tokens (seed 22); fp32 hex, row-major\n")
+        f.write(" ".join(f"{int(v):08x}" for v in lg.ravel().view(np.uint32)) + "\n")
+    print("wrote", OUT_LM)
 
 
 if __name__ == "__main__":

@@ -258,5 +258,29 @@ def pin_expert_permutation(orc):
     assert np.allclose(a["acc"], b["acc"], rtol=1e-6, atol=1e-7)
 
 
+def pin_lm_head(orc):
+    """The vocabulary projection against a float64 matmul (ragged vocabulary),
+    a one-hot token (one exact product per logit) and a zero token."""
+    H, V = 256, 333
+    w = _np(wl.lm_head_weight(V, H, seed=21))
+    x = _np(wl.tokens(3, H, seed=22))
+    lg = orc.lm_head(x, w)
+    X = f32_of_bits(x).astype(np.float64)
+    W = f32_of_bits(w).astype(np.float64)
+    ref = X @ W.T
+    bound = 1e-5 * (np.abs(X) @ np.abs(W).T) + 1e-6
+    assert lg.shape == (3, V)
+    assert np.all(np.abs(lg - ref) <= bound), "lm_head != float64 matmul"
+    c = 0x3FC0                                # bf16 1.5
+    oh = np.zeros((2, H), np.uint16)
+    oh[0, 7] = c
+    oh[1, H - 1] = c
+    lo = orc.lm_head(oh, w)
+    assert np.array_equal(lo[0], (1.5 * W[:, 7]).astype(np.float32)), "one-hot token: column 7"
+    assert np.array_equal(lo[1], (1.5 * W[:, H - 1]).astype(np.float32)), "one-hot token: last column"
+    assert not np.any(orc.lm_head(np.zeros((1, H), np.uint16), w)), "zero token"
+
+
 ALL_PINS = [pin_bf16_rounding, pin_router_logits, pin_topk_brute_force, pin_swiglu,
-            pin_dense_bruteforce, pin_one_hot_router, pin_special_cases, pin_expert_permutation]
+            pin_dense_bruteforce, pin_one_hot_router, pin_special_cases, pin_expert_permutation,
+            pin_lm_head]

@@ -38,3 +38,12 @@ def test_oracle_matches_committed_record(oracle):
         # libm exp may differ by an ulp across hosts: allow one bf16 step
         d = np.abs(res["out"].ravel().astype(np.int64) - rec["out"].astype(np.int64))
         assert d.max() <= 1 and np.mean(d == 0) > 0.99
+
+
+def test_oracle_lm_head_matches_committed_record(oracle):
+    path = os.path.join(os.path.dirname(GOLDEN), "lm_head_seed21.txt")
+    vals = [l for l in open(path) if not l.startswith("#") and l.strip()][0].split()
+    want = np.array([int(v, 16) for v in vals], np.uint32).view(np.float32).reshape(2, 333)
+    got = oracle.lm_head(wl.bf16_bits(wl.tokens(2, 256, seed=22)), wl.bf16_bits(wl.lm_head_weight(333, 256, seed=21)))
+    # fp32 sums in a fixed order, no transcendental: the same on every host
+    assert np.array_equal(got, want)

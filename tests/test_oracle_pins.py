@@ -43,6 +43,10 @@ MUTANTS = {
                           "float wv = oracle_bf16_to_f32(w_router[((size_t)h * E + e) % ((size_t)E * H)]);"),
     "softmax_shift_missing_in_sum": ("for (int e = 0; e < E; ++e) z = z + std::exp(l[e] - lmax);",
                                      "for (int e = 0; e < E; ++e) z = z + std::exp(l[e]);"),
+    "lm_head_transposed": ("const uint16_t* wr = w + (size_t)v * H;",
+                           "const uint16_t* wr = w + ((size_t)v % (size_t)H) * H;"),
+    "lm_head_last_term_dropped": ("for (int k = 0; k < H; ++k) acc",
+                                  "for (int k = 0; k + 1 < H; ++k) acc"),
 }
 
 

@@ -40,6 +40,9 @@ LING = LayerShape(hidden=2560, n_experts=512, topk=8, inter=512)
 # activated expert (the partial outputs are summed across GPUs afterwards).
 LING_TP4 = LayerShape(hidden=2560, n_experts=512, topk=8, inter=128)
 SHAPES = {"ling": LING, "ling_tp4": LING_TP4}
+# The model's vocabulary projection: hidden 2560 and "about 157k" tokens (the
+# pages give no exact count; 157,184 is the multiple of 128 nearest 157k).
+LM_HEAD_VOCAB = 157184
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -73,6 +76,19 @@ def layer_weights(shape: LayerShape, seed: int, device="cpu", std: float = WEIGH
         w_gu = _randn_bf16((E, 2 * I, H), std, g, device)
         w_d = _randn_bf16((E, H, I), std, g, device)
     return w_r, w_gu, w_d
+
+
+def lm_head_weight(vocab: int, hidden: int, seed: int, device="cpu", std: float = WEIGHT_STD) -> torch.Tensor:
+    """W [vocab, hidden] bf16 ~ N(0, std) from one generator (on CUDA in blocks
+    of 8192 rows to bound temporaries)."""
+    g = _gen(seed, device)
+    if not str(device).startswith("cuda"):
+        return _randn_bf16((vocab, hidden), std, g, device)
+    w = torch.empty((vocab, hidden), dtype=torch.bfloat16, device=device)
+    for r in range(0, vocab, 8192):
+        n = min(8192, vocab - r)
+        w[r:r + n] = _randn_bf16((n, hidden), std, g, device)
+    return w
 
 
 def tokens(M: int, hidden: int, seed: int, device="cpu") -> torch.Tensor:
