@@ -17,6 +17,7 @@ with a barrier and a device synchronize on both sides; max over ranks.
     python bench.py --shape ling_tp4      # the per-GPU slice of a 4-way TP split (inter 128)
     python bench.py --impl reference     # the CPU oracle on the same workload
     python bench.py --sweep               # M x routing sweep (writes JSON lines)
+    python bench.py --lm-head [--M 1]     # the bf16 vocabulary projection
 """
 from __future__ import annotations
 
@@ -553,6 +554,89 @@ def run_sweep(args):
     wkl.close()
 
 
+def run_lm_head(args):
+    """The vocabulary projection (include/lm_head.h), timed like the layer:
+    calls captured into CUDA graphs (PDL intact), two distinct weight copies
+    cycled (together far above L2) and a fresh x per call.  One JSON line."""
+    import torch
+    from weight_streaming_expert_gb300 import LmHead
+    from weight_streaming_expert_gb300 import workloads as wl
+    rank, ws, local, pg = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    H = wl.LING.hidden
+    V = wl.LM_HEAD_VOCAB // (4 if args.shape == "ling_tp4" else 1)
+    M = min(args.M, 16)
+    heads = [LmHead(wl.lm_head_weight(V, H, seed=5000 + i, device=dev)) for i in range(2)]
+    torch.cuda.empty_cache()
+    xs = [wl.tokens(M, H, seed=1_000_000 + i, device=dev) for i in range(args.pool)]
+    outs = [torch.empty((M, V), dtype=torch.float32, device=dev) for _ in range(2)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    call = lambda c: heads[c % 2](xs[c % len(xs)], outs[c % 2], stream=s)
+    with torch.cuda.stream(s):
+        for c in range(args.warmup):
+            call(c)
+    s.synchronize()
+    G = min(64, args.steps)
+    full, rem = divmod(args.steps, G)
+    graphs = []
+    for n in ([G] if full else []) + ([rem] if rem else []):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for c in range(n):
+                    call(c)
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(full):
+            graphs[0].replay()
+        if rem:
+            graphs[-1].replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    barrier(pg)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.steps)
+    status = max(h.status() for h in heads)
+    for h in heads:
+        h.close()
+    bytes_call = V * H * 2 + M * H * 2 + M * V * 4
+    us = ms * 1000.0
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "cold-L2 \u00b5s per lm_head call and achieved HBM GB/s (% of GB300 peak)",
+            "value": round(us, 3), "unit": "\u00b5s/call", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic: seeded N(0,0.02) bf16 weight, N(0,1) bf16 tokens",
+            "config": {"workload": f"bf16 lm_head GEMV: hidden {H}, vocab {V}"
+                                   f"{' (vocab-parallel quarter)' if args.shape == 'ling_tp4' else ''}, M={M}, fp32 logits",
+                       "M": M, "weights_cycled": 2,
+                       "l2_policy": f"inputs larger than L2: 2 weight copies of {V * H * 2 / 1e6:.0f} MB cycled, fresh x per call",
+                       "graph_calls": G, "parallelism": f"replicas x{ws}"},
+            "achieved_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
+            "algorithmic_bytes_per_call": int(bytes_call), "device_status": status,
+            "roofline": {"bound": "hbm", "kernel": "lm_head_kernel", "achieved": round(gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None,
+                         "algorithmic_bytes_per_launch": int(bytes_call), "peak_kind": peak_kind},
+            "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,11 +655,15 @@ def main(argv=None):
                     help="skip the M=1 and M=16 (Zipf) side measurements")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle timing")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--lm-head", dest="lm_head", action="store_true",
+                    help="time the bf16 vocabulary projection (hidden 2560, vocab 157,184; M <= 16) instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.lm_head:
+        run_lm_head(args)
     elif args.sweep:
         run_sweep(args)
     else:

@@ -9,11 +9,12 @@ import pytest
 from weight_streaming_expert_gb300 import build_lib, native
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "moe.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = "\n".join(open(h).read() for h in HEADERS)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
     names = re.findall(r"\b(moe_[a-z_]+)\s*\(", src)
@@ -28,7 +29,8 @@ def L():
 
 def test_header_declares_the_layer_calls():
     names = declared_functions()
-    for n in ("moe_create", "moe_forward", "moe_destroy"):
+    for n in ("moe_create", "moe_forward", "moe_destroy",
+              "moe_lm_head_create", "moe_lm_head_forward", "moe_lm_head_destroy"):
         assert n in names
 
 
@@ -86,3 +88,22 @@ def test_no_gpu_create_fails_cleanly(L):
     h = L.moe_create(256, 16, 2, 128, dummy, dummy, dummy)
     assert not h
     assert native.last_error()
+
+
+@pytest.mark.parametrize("hidden,vocab,frag", [(255, 1000, "hidden"), (2816, 1000, "hidden"),
+                                               (2560, 0, "vocab"), (2560, (1 << 24) + 1, "vocab")])
+def test_lm_head_create_rejects_bad_sizes(L, hidden, vocab, frag):
+    assert not L.moe_lm_head_create(hidden, vocab, ctypes.c_void_p(16))
+    assert frag in native.last_error()
+
+
+def test_lm_head_rejects_null_and_misaligned_weights(L):
+    assert not L.moe_lm_head_create(2560, 1000, None)
+    assert not L.moe_lm_head_create(2560, 1000, ctypes.c_void_p(24))
+    assert "aligned" in native.last_error()
+
+
+def test_lm_head_forward_rejects_null_handle(L):
+    assert L.moe_lm_head_forward(None, None, None, 1, None) == native.MOE_ERR_INVALID_ARG
+    assert L.moe_lm_head_get_status(None) == native.MOE_ERR_INVALID_ARG
+    L.moe_lm_head_destroy(None)  # no-op

@@ -2,15 +2,19 @@
 
 The layer (router GEMV -> softmax top-k -> SwiGLU experts -> weighted
 combine) runs in hand-written sm_103a CUDA kernels behind the C ABI in
-``include/moe.h``; ``MoELayer`` is its Python face.  Importing the package
+``include/moe.h``; ``MoELayer`` is its Python face.  ``LmHead`` is the bf16
+vocabulary projection of the same decode step (``include/lm_head.h``).  Importing the package
 loads nothing; the CUDA library is loaded (and must exist) on first use.
 """
 
-__all__ = ["MoELayer"]
+__all__ = ["MoELayer", "LmHead"]
 
 
 def __getattr__(name):
     if name == "MoELayer":
         from .layer import MoELayer
         return MoELayer
+    if name == "LmHead":
+        from .layer import LmHead
+        return LmHead
     raise AttributeError(name)

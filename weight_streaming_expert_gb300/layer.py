@@ -137,3 +137,47 @@ class MoELayer:
             self.close()
         except Exception:
             pass
+
+
+class LmHead:
+    """The bf16 vocabulary projection (``include/lm_head.h``): fp32 logits
+    [M, V] = x [M, H] @ W [V, H]^T for M <= 16.  W (bf16, contiguous, on the
+    current CUDA device) is copied into the library at construction."""
+
+    def __init__(self, w):
+        if w.dtype != torch.bfloat16 or not w.is_cuda or not w.is_contiguous() or w.dim() != 2:
+            raise ValueError("w must be a contiguous bf16 CUDA tensor [vocab, hidden]")
+        self.vocab, self.hidden = w.shape
+        self.device = w.device
+        with torch.cuda.device(self.device):
+            h = N.lib().moe_lm_head_create(self.hidden, self.vocab, _ptr(w))
+        if not h:
+            raise N.MoEError("moe_lm_head_create", N.MOE_ERR_INVALID_ARG, N.last_error())
+        self._h = ctypes.c_void_p(h)
+
+    def __call__(self, x, logits=None, stream=None):
+        return self.forward(x, logits, stream)
+
+    def forward(self, x, logits=None, stream=None):
+        """x: bf16 [M, H] CUDA.  Returns fp32 logits [M, V]."""
+        if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.shape[1] != self.hidden:
+            raise ValueError("x must be contiguous bf16 [M, hidden]")
+        if logits is None:
+            logits = torch.empty((x.shape[0], self.vocab), dtype=torch.float32, device=x.device)
+        rc = N.lib().moe_lm_head_forward(self._h, _ptr(x), _ptr(logits), x.shape[0], _stream_ptr(stream))
+        N.check("moe_lm_head_forward", rc)
+        return logits
+
+    def status(self) -> int:
+        return N.lib().moe_lm_head_get_status(self._h)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            N.lib().moe_lm_head_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

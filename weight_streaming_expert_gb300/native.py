@@ -1,4 +1,5 @@
-"""ctypes binding of include/moe.h (same names; argument marshalling only).
+"""ctypes binding of include/moe.h and include/lm_head.h (same names; argument
+marshalling only).
 
 Every step of the layer runs in the CUDA library ``_build/libwse.so``.  There
 is no Python or CPU fallback: if the library is missing or fails to load,
@@ -22,6 +23,7 @@ MOE_ERR_CUDA = 3
 MOE_ERR_OOM = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
 MOE_MAX_TOKENS = 64
+MOE_LM_HEAD_MAX_TOKENS = 16
 MOE_FWD_NO_PDL = 0x1
 MOE_FWD_GRAPH = 0x2
 MOE_FWD_TRACE = 0x4
@@ -89,6 +91,14 @@ def lib(build_if_missing: bool = True):
         L.moe_route_static.restype = ci
         L.moe_destroy.argtypes = [vp]
         L.moe_destroy.restype = None
+        L.moe_lm_head_create.argtypes = [ci, ci, vp]
+        L.moe_lm_head_create.restype = vp
+        L.moe_lm_head_forward.argtypes = [vp, vp, vp, ci, vp]
+        L.moe_lm_head_forward.restype = ci
+        L.moe_lm_head_get_status.argtypes = [vp]
+        L.moe_lm_head_get_status.restype = ci
+        L.moe_lm_head_destroy.argtypes = [vp]
+        L.moe_lm_head_destroy.restype = None
         L.moe_last_error.argtypes = []
         L.moe_last_error.restype = ctypes.c_char_p
         _lib = L
