@@ -209,46 +209,67 @@ int oracle_expert_down(int H, int I, const uint16_t* h_row,
 
 // -------------------------------------------------------------- layer ----
 
-// The whole layer for M tokens.
+// The whole layer for M tokens, with the layer variants the post's model
+// uses ("Two kinds of idle": a 513-expert decode, i.e. a shared expert fused
+// next to the 512 routed ones; "PDL: ...": the combine is an fp32 sum times a
+// scale; "the router top-k prefetches its bias").
 //   x         [M][H] bf16           w_router  [E][H] bf16
 //   bias      [E] fp32 or NULL      w_gate_up [E][2I][H] bf16
 //   w_down    [E][H][I] bf16
+//   bias_selection_only: 0 -> the bias shifts the logits used for both the
+//             selection and the weights; 1 -> it shifts only the selection,
+//             the weights are the softmax of the unbiased logits,
+//             renormalised over the chosen k.
+//   w_shared_gate_up [2I][H], w_shared_down [H][I] bf16, or both NULL: a
+//             shared expert every token passes through with weight 1.
+//   routed_scale  multiplies every routed weight (1 = none).
 //   idx_in    [M][K] or NULL: when given, these experts are used instead of
 //             the oracle's own selection and weighted with the oracle's
 //             renormalised softmax over that set (near-tie scoring).
+// The combine: acc = sum over slots s < K (in order) of (scale * w_s) * y_s,
+// then + y_shared; out = bf16(acc), one rounding.
 // Outputs (any may be NULL except out):
-//   logits [M][E] fp32, idx [M][K] int32, w [M][K] fp32,
-//   acc    [M][H] fp32 (the combine before the final cast),
-//   h      [M][K][I] bf16 (activated intermediate rows),
-//   out    [M][H] bf16.
-int oracle_moe_forward(int M, int H, int E, int K, int I, const uint16_t* x,
-                       const uint16_t* w_router, const float* bias,
-                       const uint16_t* w_gate_up, const uint16_t* w_down,
-                       const int32_t* idx_in, float* logits_out,
-                       int32_t* idx_out, float* w_out, float* acc_out,
-                       uint16_t* h_out, uint16_t* out) {
+//   logits [M][E] fp32 (the selection logits), idx [M][K] int32,
+//   w [M][K] fp32 (renormalised, unscaled), acc [M][H] fp32 (the combine
+//   before the final cast), h [M][K][I] bf16 (routed intermediate rows),
+//   out [M][H] bf16.
+int oracle_moe_forward_ex(int M, int H, int E, int K, int I, const uint16_t* x,
+                          const uint16_t* w_router, const float* bias, int bias_selection_only,
+                          const uint16_t* w_gate_up, const uint16_t* w_down,
+                          const uint16_t* w_shared_gate_up, const uint16_t* w_shared_down,
+                          float routed_scale, const int32_t* idx_in, float* logits_out,
+                          int32_t* idx_out, float* w_out, float* acc_out,
+                          uint16_t* h_out, uint16_t* out) {
   if (M < 0 || H <= 0 || E <= 0 || K <= 0 || K > E || I <= 0) return 1;
   if (!x || !w_router || !w_gate_up || !w_down || !out) return 1;
+  if ((w_shared_gate_up == nullptr) != (w_shared_down == nullptr)) return 1;
   if (M == 0) return 0;
-  std::vector<float> logits((size_t)M * E);
+  const bool sel_only = bias_selection_only && bias;
+  std::vector<float> logits((size_t)M * E), unbiased;
   std::vector<int32_t> idx((size_t)M * K);
   std::vector<float> w((size_t)M * K);
   if (oracle_router_logits(M, H, E, x, w_router, bias, logits.data())) return 1;
+  if (sel_only) {
+    unbiased.resize((size_t)M * E);
+    if (oracle_router_logits(M, H, E, x, w_router, nullptr, unbiased.data())) return 1;
+  }
+  const float* wlog = sel_only ? unbiased.data() : logits.data();  // logits the weights come from
   if (idx_in) {
-    for (int m = 0; m < M; ++m) {
+    for (int m = 0; m < M; ++m)
       for (int j = 0; j < K; ++j) idx[(size_t)m * K + j] = idx_in[(size_t)m * K + j];
-      if (oracle_weights_for_set(E, K, logits.data() + (size_t)m * E,
-                                 idx.data() + (size_t)m * K,
-                                 w.data() + (size_t)m * K))
-        return 1;
-    }
   } else {
     oracle_topk_softmax(M, E, K, logits.data(), idx.data(), w.data());
   }
+  if (idx_in || sel_only) {
+    for (int m = 0; m < M; ++m)
+      if (oracle_weights_for_set(E, K, wlog + (size_t)m * E, idx.data() + (size_t)m * K,
+                                 w.data() + (size_t)m * K))
+        return 1;
+  }
   std::vector<uint16_t> h(I);
   std::vector<float> y(H);
+  std::vector<float> ys(H);
   std::vector<float> acc(H);
-  const float scale = 1.0f;
   for (int m = 0; m < M; ++m) {
     const uint16_t* xr = x + (size_t)m * H;
     for (int j = 0; j < H; ++j) acc[j] = 0.0f;
@@ -258,11 +279,16 @@ int oracle_moe_forward(int M, int H, int E, int K, int I, const uint16_t* x,
       if (h_out)
         for (int r = 0; r < I; ++r) h_out[((size_t)m * K + s) * I + r] = h[r];
       oracle_expert_down(H, I, h.data(), w_down + (size_t)e * H * I, y.data());
-      float ws = w[(size_t)m * K + s];
+      float ws = routed_scale * w[(size_t)m * K + s];
       for (int j = 0; j < H; ++j) acc[j] = acc[j] + ws * y[j];
     }
+    if (w_shared_gate_up) {
+      oracle_expert_swiglu(H, I, xr, w_shared_gate_up, h.data());
+      oracle_expert_down(H, I, h.data(), w_shared_down, ys.data());
+      for (int j = 0; j < H; ++j) acc[j] = acc[j] + ys[j];
+    }
     for (int j = 0; j < H; ++j) {
-      float v = scale * acc[j];
+      float v = acc[j];
       if (acc_out) acc_out[(size_t)m * H + j] = v;
       out[(size_t)m * H + j] = oracle_f32_to_bf16(v);
     }
@@ -271,6 +297,18 @@ int oracle_moe_forward(int M, int H, int E, int K, int I, const uint16_t* x,
   if (idx_out) std::memcpy(idx_out, idx.data(), idx.size() * 4);
   if (w_out) std::memcpy(w_out, w.data(), w.size() * 4);
   return 0;
+}
+
+// The plain layer: no shared expert, scale 1, the bias (if any) on the
+// logits for both selection and weights.
+int oracle_moe_forward(int M, int H, int E, int K, int I, const uint16_t* x,
+                       const uint16_t* w_router, const float* bias,
+                       const uint16_t* w_gate_up, const uint16_t* w_down,
+                       const int32_t* idx_in, float* logits_out,
+                       int32_t* idx_out, float* w_out, float* acc_out,
+                       uint16_t* h_out, uint16_t* out) {
+  return oracle_moe_forward_ex(M, H, E, K, I, x, w_router, bias, 0, w_gate_up, w_down, nullptr, nullptr,
+                               1.0f, idx_in, logits_out, idx_out, w_out, acc_out, h_out, out);
 }
 
 }  // extern "C"

@@ -61,8 +61,11 @@ def load(path: str | None = None):
         lib.oracle_moe_forward.argtypes = [ci, ci, ci, ci, ci, u16p, u16p, f32p, u16p, u16p,
                                            i32p, f32p, i32p, f32p, f32p, u16p, u16p]
         lib.oracle_lm_head.argtypes = [ci, ci, ci, u16p, u16p, f32p]
+        lib.oracle_moe_forward_ex.argtypes = [ci, ci, ci, ci, ci, u16p, u16p, f32p, ci, u16p, u16p, u16p, u16p,
+                                              ctypes.c_float, i32p, f32p, i32p, f32p, f32p, u16p, u16p]
         for name in ("oracle_router_logits", "oracle_topk_softmax", "oracle_weights_for_set",
-                     "oracle_expert_swiglu", "oracle_expert_down", "oracle_moe_forward", "oracle_lm_head"):
+                     "oracle_expert_swiglu", "oracle_expert_down", "oracle_moe_forward", "oracle_lm_head",
+                     "oracle_moe_forward_ex"):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
@@ -163,8 +166,11 @@ class Oracle:
         return y
 
     # whole layer ---------------------------------------------------------
-    def moe_forward(self, x, w_router, w_gate_up, w_down, k, bias=None, idx_in=None, want_h=False):
-        """Returns dict(out=u16[M,H], acc=f32[M,H], logits, idx, w, h?)."""
+    def moe_forward(self, x, w_router, w_gate_up, w_down, k, bias=None, idx_in=None, want_h=False,
+                    shared_gate_up=None, shared_down=None, routed_scale=1.0, bias_selection_only=False):
+        """Returns dict(out=u16[M,H], acc=f32[M,H], logits, idx, w, h?).  The
+        layer variants: a shared expert (shared_gate_up [2I,H], shared_down
+        [H,I]), a routed scaling factor, a bias for the selection only."""
         x, w_router, w_gate_up, w_down = _u16(x), _u16(w_router), _u16(w_gate_up), _u16(w_down)
         M, H = x.shape
         E = w_router.shape[0]
@@ -172,6 +178,10 @@ class Oracle:
         assert w_router.shape == (E, H)
         assert w_gate_up.shape == (E, 2 * I, H)
         assert w_down.shape == (E, H, I)
+        sg = None if shared_gate_up is None else _u16(shared_gate_up)
+        sd = None if shared_down is None else _u16(shared_down)
+        if sg is not None:
+            assert sg.shape == (2 * I, H) and sd is not None and sd.shape == (H, I)
         logits = np.zeros((M, E), np.float32)
         idx = np.zeros((M, k), np.int32)
         w = np.zeros((M, k), np.float32)
@@ -180,9 +190,10 @@ class Oracle:
         h = np.zeros((M, k, I), np.uint16) if want_h else None
         b = None if bias is None else np.ascontiguousarray(bias, np.float32)
         ii = None if idx_in is None else np.ascontiguousarray(idx_in, np.int32)
-        rc = self.lib.oracle_moe_forward(
+        rc = self.lib.oracle_moe_forward_ex(
             M, H, E, k, I, _p(x, ctypes.c_uint16), _p(w_router, ctypes.c_uint16), _p(b, ctypes.c_float),
-            _p(w_gate_up, ctypes.c_uint16), _p(w_down, ctypes.c_uint16), _p(ii, ctypes.c_int32),
+            1 if bias_selection_only else 0, _p(w_gate_up, ctypes.c_uint16), _p(w_down, ctypes.c_uint16),
+            _p(sg, ctypes.c_uint16), _p(sd, ctypes.c_uint16), float(routed_scale), _p(ii, ctypes.c_int32),
             _p(logits, ctypes.c_float), _p(idx, ctypes.c_int32), _p(w, ctypes.c_float),
             _p(acc, ctypes.c_float), _p(h, ctypes.c_uint16), _p(out, ctypes.c_uint16))
         assert rc == 0, "oracle rejected its arguments"

@@ -281,6 +281,69 @@ def pin_lm_head(orc):
     assert not np.any(orc.lm_head(np.zeros((1, H), np.uint16), w)), "zero token"
 
 
+def _shared_weights(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    H, I = shape.hidden, shape.inter
+    sgu = (torch.randn(2 * I, H, generator=g) * wl.WEIGHT_STD).to(torch.bfloat16)
+    sd = (torch.randn(H, I, generator=g) * wl.WEIGHT_STD).to(torch.bfloat16)
+    return _np(sgu), _np(sd)
+
+
+def _dense_mlp(x, w_gu, w_d):
+    """float64 SwiGLU MLP with h rounded to bf16 (library rounding)."""
+    I = w_d.shape[1]
+    X = f32_of_bits(x).astype(np.float64)
+    Wg = f32_of_bits(w_gu[:I]).astype(np.float64)
+    Wu = f32_of_bits(w_gu[I:]).astype(np.float64)
+    Wd = f32_of_bits(w_d).astype(np.float64)
+    hh = silu64(X @ Wg.T) * (X @ Wu.T)
+    hh = f32_of_bits(bf16_round_torch(hh.astype(np.float32))).astype(np.float64)
+    return hh @ Wd.T
+
+
+def pin_shared_expert_and_scale(orc):
+    """Shared expert + routed scale against the dense brute force: acc =
+    scale * (routed mixture) + shared MLP; scale 0 leaves the shared MLP
+    alone; no shared expert and scale 1 is the plain layer, bit for bit."""
+    shape = wl.TINY
+    x, w_r, w_gu, w_d = tiny(M=4, seed=12)
+    sgu, sd = _shared_weights(shape, 13)
+    shared = _dense_mlp(x, sgu, sd)
+    _, routed, _ = dense_reference(x, w_r, w_gu, w_d, shape.topk)
+    for scale in (0.0, 1.0, 2.5):
+        r = orc.moe_forward(x, w_r, w_gu, w_d, shape.topk, shared_gate_up=sgu, shared_down=sd, routed_scale=scale)
+        assert rel_l2(r["acc"], scale * routed + shared) < 2e-3, f"shared + {scale} x routed != dense brute force"
+    r0 = orc.moe_forward(x, w_r, w_gu, w_d, shape.topk, shared_gate_up=sgu, shared_down=sd, routed_scale=0.0)
+    assert rel_l2(r0["acc"], shared) < 2e-3, "scale 0: the shared expert alone"
+    plain = orc.moe_forward(x, w_r, w_gu, w_d, shape.topk)
+    same = orc.moe_forward(x, w_r, w_gu, w_d, shape.topk, routed_scale=1.0)
+    assert np.array_equal(plain["out"], same["out"]) and np.array_equal(plain["acc"], same["acc"])
+
+
+def pin_selection_only_bias(orc):
+    """The bias picks the experts, the unbiased softmax weighs them (numpy
+    lexsort and a float64 softmax over the chosen set)."""
+    shape = wl.TINY
+    x, w_r, w_gu, w_d = tiny(M=5, seed=14)
+    E, k = shape.n_experts, shape.topk
+    b = (np.random.default_rng(15).standard_normal(E) * 0.5).astype(np.float32)
+    r = orc.moe_forward(x, w_r, w_gu, w_d, k, bias=b, bias_selection_only=True)
+    X = f32_of_bits(x).astype(np.float64)
+    Wr = f32_of_bits(w_r).astype(np.float64)
+    lg = X @ Wr.T
+    moved = 0
+    for m in range(x.shape[0]):
+        sel = lg[m] + b
+        order = np.lexsort((np.arange(E), -sel))[:k]
+        assert np.array_equal(r["idx"][m], order), "selection must follow the biased logits"
+        p = np.exp(lg[m][order] - lg[m][order].max())
+        assert np.allclose(r["w"][m], p / p.sum(), rtol=1e-5, atol=1e-7), "weights: unbiased softmax over the set"
+        moved += not np.array_equal(order, np.lexsort((np.arange(E), -lg[m]))[:k])
+    assert moved > 0, "the bias must change some token's selection in this case"
+    rb = orc.moe_forward(x, w_r, w_gu, w_d, k, bias=b)
+    assert not np.allclose(rb["w"], r["w"]), "the two bias modes must weigh differently"
+
+
 ALL_PINS = [pin_bf16_rounding, pin_router_logits, pin_topk_brute_force, pin_swiglu,
             pin_dense_bruteforce, pin_one_hot_router, pin_special_cases, pin_expert_permutation,
-            pin_lm_head]
+            pin_lm_head, pin_shared_expert_and_scale, pin_selection_only_bias]

@@ -37,7 +37,7 @@ MUTANTS = {
                         "for (int r = 0; r < I; ++r)\n"
                         "      acc = acc + oracle_bf16_to_f32(h_row[r]) * oracle_bf16_to_f32(w_down_e[(size_t)r * H + (j % H)] );"),
     "bias_dropped": ("if (bias) acc = acc + bias[e];", "(void)bias;"),
-    "first_slot_weight": ("float ws = w[(size_t)m * K + s];", "float ws = w[(size_t)m * K];"),
+    "first_slot_weight": ("float ws = routed_scale * w[(size_t)m * K + s];", "float ws = routed_scale * w[(size_t)m * K];"),
     "truncating_round": ("u += 0x7FFFu + lsb;", "(void)lsb;"),
     "router_transposed": ("float wv = oracle_bf16_to_f32(w_router[(size_t)e * H + h]);",
                           "float wv = oracle_bf16_to_f32(w_router[((size_t)h * E + e) % ((size_t)E * H)]);"),
@@ -47,6 +47,10 @@ MUTANTS = {
                            "const uint16_t* wr = w + ((size_t)v % (size_t)H) * H;"),
     "lm_head_last_term_dropped": ("for (int k = 0; k < H; ++k) acc",
                                   "for (int k = 0; k + 1 < H; ++k) acc"),
+    "shared_expert_dropped": ("for (int j = 0; j < H; ++j) acc[j] = acc[j] + ys[j];", "(void)ys;"),
+    "routed_scale_ignored": ("float ws = routed_scale * w[(size_t)m * K + s];", "float ws = w[(size_t)m * K + s];"),
+    "selection_weights_from_biased_logits": ("const float* wlog = sel_only ? unbiased.data() : logits.data();",
+                                             "const float* wlog = logits.data();"),
 }
 
 
