@@ -168,7 +168,7 @@ def max_over_ranks(pg, v):
 class Workload:
     """Distinct layers on the device plus pools of token batches."""
 
-    def __init__(self, shape, n_layers, M, pool, zipf, device, layer_seed0=1000):
+    def __init__(self, shape, n_layers, M, pool, zipf, device, layer_seed0=1000, variant=False):
         import torch
         from weight_streaming_expert_gb300 import MoELayer
         from weight_streaming_expert_gb300 import workloads as wl
@@ -176,8 +176,17 @@ class Workload:
         self.layers = []
         for l in range(n_layers):
             w_r, w_gu, w_d = wl.layer_weights(shape, seed=layer_seed0 + l, device=device)
-            self.layers.append(MoELayer(w_r, w_gu, w_d, topk=shape.topk))
-            del w_r, w_gu, w_d
+            kw = {}
+            if variant:  # a shared expert, routed scale 2.5, the bias for selection only
+                g = torch.Generator(device=device).manual_seed(layer_seed0 + 500 + l)
+                H, I = shape.hidden, shape.inter
+                kw = dict(shared_gate_up=(torch.randn(2 * I, H, generator=g, device=device) * wl.WEIGHT_STD)
+                          .to(torch.bfloat16),
+                          shared_down=(torch.randn(H, I, generator=g, device=device) * wl.WEIGHT_STD)
+                          .to(torch.bfloat16),
+                          routed_scale=2.5, bias_selection_only=True)
+            self.layers.append(MoELayer(w_r, w_gu, w_d, topk=shape.topk, **kw))
+            del w_r, w_gu, w_d, kw
             torch.cuda.empty_cache()
         self.set_routing(zipf)
         self.new_pool(M, pool)
@@ -417,10 +426,10 @@ def run_ours(args):
     shape = wl.SHAPES[args.shape]
     M = args.M
     n_layers = n_layers_for(M, shape, l2, args.layers)
-    wkl = Workload(shape, n_layers, M, args.pool, args.zipf, dev)
+    wkl = Workload(shape, n_layers, M, args.pool, args.zipf, dev, variant=args.variant)
     ms, active, clocks = time_graph(wkl, args.steps, args.warmup, pg, sample_clocks=(rank == 0),
                                     gpu_index=local)
-    mean_active = float(np.mean(active))
+    mean_active = float(np.mean(active)) + (1.0 if args.variant else 0.0)  # + the shared expert
     bytes_call = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, mean_active)
     us = ms * 1000.0
     gbs = bytes_call / (us * 1e-6) / 1e9
@@ -433,7 +442,7 @@ def run_ours(args):
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
         if (tr.get("source_hash") == source_hash(LAYER_SOURCES) and tr.get("M") == M
-                and args.shape == tr.get("shape", "ling")):
+                and args.shape == tr.get("shape", "ling") and not args.variant):
             # measured on a smaller run (one layer, 8 calls): DRAM traffic
             # follows the algorithmic bytes, so scale it to this run's launches
             traffic = int(round(tr["bytes_per_launch"] * bytes_call / tr["algorithmic_bytes_per_launch"]))
@@ -447,6 +456,7 @@ def run_ours(args):
             wkl.set_routing(z2)
             wkl.new_pool(m2, args.pool)
             ms2, act2, _ = time_graph(wkl, min(args.steps, 4000), args.warmup, None)
+            act2 = [a + (1 if args.variant else 0) for a in act2]
             b2 = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, m2, float(np.mean(act2)))
             by_m[f"M={m2}" + ("_zipf" if z2 else "")] = {
                 "us_per_call": round(ms2 * 1000, 3), "achieved_gbs": round(b2 / (ms2 * 1e-3) / 1e9, 1),
@@ -473,6 +483,7 @@ def run_ours(args):
                                    f"{' (per-GPU slice of a 4-way TP split)' if args.shape == 'ling_tp4' else ''}: "
                                    f"hidden {shape.hidden}, {shape.n_experts} experts, top-{shape.topk} softmax+renorm, "
                                    f"SwiGLU inter {shape.inter}, "
+                                   f"{'+ shared expert, routed scale 2.5, bias for selection only, ' if args.variant else ''}"
                                    f"M={M}, {'Zipf(1.1) router bias' if args.zipf else 'uniform routing'}",
                        "M": M, "layers_cycled": n_layers, "x_pool": args.pool,
                        "l2_policy": f"inputs larger than L2: {n_layers} distinct layer weight sets cycled, "
@@ -655,6 +666,8 @@ def main(argv=None):
                     help="skip the M=1 and M=16 (Zipf) side measurements")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle timing")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--variant", action="store_true",
+                    help="layers with a shared expert, routed scale 2.5 and the router bias for selection only")
     ap.add_argument("--lm-head", dest="lm_head", action="store_true",
                     help="time the bf16 vocabulary projection (hidden 2560, vocab 157,184; M <= 16) instead")
     args = ap.parse_args(argv)

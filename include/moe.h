@@ -109,6 +109,41 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter,
                         const void* w_down);
 
 /*
+ * Layer variants of the post's model (zero-initialise, then set fields):
+ *   - a shared expert every token passes with weight 1, fused as one more
+ *     bucket next to the routed experts ("a 513-expert decode", section "Two
+ *     kinds of idle"), with the routed experts' inter size;
+ *   - a routed scaling factor: the combine is an fp32 sum times a scale
+ *     ("PDL: ..."), here a factor on every routed weight;
+ *   - a router bias that chooses the experts without weighing them (the
+ *     router top-k "prefetches its bias").
+ * Combine per token: out = bf16( sum over slots j < k, in order, of
+ * (routed_scale * w_j) * y_j, then + y_shared ), one rounding.
+ */
+typedef struct {
+  const void* w_shared_gate_up; /* device bf16 [2I][H] (gate rows first), 16-byte
+                                   aligned, or NULL: no shared expert */
+  const void* w_shared_down;    /* device bf16 [H][I], or NULL (both or neither) */
+  float routed_scale;           /* factor on every routed weight; <= 0 means 1 */
+  int bias_selection_only;      /* 1: moe_set_router_bias's bias picks the
+                                   experts only; the weights are the softmax of
+                                   the unbiased logits renormalised over the k.
+                                   0: the bias shifts the logits for both. */
+} moe_layer_opts_t;
+
+/*
+ * moe_create_ex -- moe_create with the layer variants (opts NULL: none).
+ * The shared expert's weights are copied and re-laid out like the routed
+ * ones.  topk_idx / topk_w of the forward calls hold the routed experts
+ * only (topk_w unscaled); moe_read_routing also lists the shared expert's
+ * pairs (pair M*k + m of token m, expert id n_experts, weight 1) and its
+ * pair_w values include the scale.  Errors as moe_create.
+ */
+moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter,
+                           const void* w_router, const void* w_gate_up,
+                           const void* w_down, const moe_layer_opts_t* opts);
+
+/*
  * moe_forward -- run the layer on M tokens, asynchronously on `stream`.
  *   x         device bf16 [M][H], 16-byte aligned, read only.
  *   out       device bf16 [M][H]: out[m] = bf16( sum_j w[m][j] * y_j ),
@@ -186,6 +221,9 @@ typedef struct {
   int kernels_per_forward; /* kernel launches per forward call (1) */
   int router_split;        /* hidden-dim split of the router matvec units */
   size_t smem_bytes;       /* dynamic shared memory per CTA at M = 64 */
+  int shared_expert;       /* 1 if the layer has a shared expert */
+  float routed_scale;      /* factor on every routed weight */
+  int bias_selection_only; /* 1 if the router bias only picks the experts */
 } moe_info_t;
 
 int moe_get_info(const moe_layer_t* h, moe_info_t* out);
@@ -199,9 +237,11 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* out);
  *   n_groups, n_active   host int*: groups written, distinct experts.
  *   grp_expert, grp_start, grp_cnt   host int32 [cap]: per group its expert,
  *                        first sorted position and pair count (<= 16).
- *   pair_list            host int32 [M*k]: pair id at each sorted position.
- *   pair_w               host fp32 [M*k]: routing weight of each pair id.
- *   cap                  capacity of the grp_* arrays (>= M*k suffices).
+ *   pair_list            host int32 [NP]: pair id at each sorted position.
+ *   pair_w               host fp32 [NP]: routing weight of each pair id.
+ *   cap                  capacity of the grp_* arrays (>= NP suffices).
+ * With a shared expert NP = M*(k+1): pairs M*k .. M*k+M-1 are the shared
+ * expert's (expert id n_experts).
  */
 int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
                      int32_t* grp_expert, int32_t* grp_start, int32_t* grp_cnt,

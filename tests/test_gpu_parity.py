@@ -404,3 +404,81 @@ def test_timed_launch_matches(ling):
     torch.cuda.synchronize()
     assert torch.equal(out, ref) and torch.equal(idx, ridx)
     assert ev[0].elapsed_time(ev[1]) > 0
+
+
+# ------------------------------------------------------- layer variants --
+# A shared expert every token passes with weight 1, a routed scaling factor
+# on every routed weight, and a router bias that picks the experts without
+# weighing them (the oracle's moe_forward_ex).
+
+def shared_weights(shape, seed, device="cpu"):
+    g = torch.Generator(device=device).manual_seed(seed)
+    H, I = shape.hidden, shape.inter
+    sgu = (torch.randn(2 * I, H, generator=g, device=device) * wl.WEIGHT_STD).to(torch.bfloat16)
+    sd = (torch.randn(H, I, generator=g, device=device) * wl.WEIGHT_STD).to(torch.bfloat16)
+    return sgu, sd
+
+
+def variant_layer(MoELayer, shape, seed, scale, sel_only, device="cpu"):
+    w_r, w_gu, w_d = wl.layer_weights(shape, seed=seed, device=device)
+    sgu, sd = shared_weights(shape, seed + 1, device=device)
+    layer = MoELayer(w_r.to(DEV), w_gu.to(DEV), w_d.to(DEV), topk=shape.topk, shared_gate_up=sgu.to(DEV),
+                     shared_down=sd.to(DEV), routed_scale=scale, bias_selection_only=sel_only)
+    host = dict(wr=bits(w_r), wgu=bits(w_gu), wd=bits(w_d))
+    variant = dict(shared_gate_up=bits(sgu), shared_down=bits(sd), routed_scale=scale,
+                   bias_selection_only=sel_only)
+    return layer, host, variant
+
+
+@pytest.mark.parametrize("H,E,k,I,M,scale,sel_only", [
+    (256, 16, 2, 128, 1, 1.0, False), (256, 16, 2, 128, 5, 2.5, True), (512, 64, 6, 256, 16, 0.5, True),
+    (1280, 40, 3, 256, 23, 2.5, True), (2560, 24, 2, 512, 64, 1.0, False), (1024, 96, 8, 512, 9, 16.0, True)])
+def test_variants_small(oracle, MoELayer, H, E, k, I, M, scale, sel_only):
+    shape = wl.LayerShape(hidden=H, n_experts=E, topk=k, inter=I)
+    layer, host, variant = variant_layer(MoELayer, shape, H + E + k + 77, scale, sel_only)
+    bias = torch.from_numpy((np.random.default_rng(E).standard_normal(E) * 0.5).astype(np.float32))
+    x = wl.tokens(M, H, seed=M + 500).to(DEV)
+    run_and_check(oracle, layer, host, x, k, bias=bias, **variant)
+    run_and_check(oracle, layer, host, x, k, bias=None, **variant)
+    layer.close()
+
+
+@pytest.fixture(scope="module")
+def ling_variant(MoELayer):
+    """Full size, a shared expert, routed scale 2.5, bias for selection only."""
+    layer, host, variant = variant_layer(MoELayer, wl.LING, 1200, 2.5, True, device=DEV)
+    torch.cuda.empty_cache()
+    yield layer, host, variant
+    layer.close()
+
+
+@pytest.mark.parametrize("M,zipf", [(6, False), (1, True), (16, True), (64, False)])
+def test_ling_variants(oracle, ling_variant, M, zipf):
+    layer, host, variant = ling_variant
+    bias = wl.zipf_router_bias(wl.LING.n_experts) if zipf else None
+    x = wl.tokens(M, wl.LING.hidden, seed=6_000_000 + M, device=DEV)
+    run_and_check(oracle, layer, host, x, wl.LING.topk, bias=bias, **variant)
+
+
+def test_variant_routing_outputs(oracle, ling_variant):
+    """topk_w is the unscaled renormalised weight; the compaction lists the
+    shared expert's pairs (id E, weight 1) and the routed pairs scaled."""
+    layer, host, variant = ling_variant
+    E, k = wl.LING.n_experts, wl.LING.topk
+    M = 6
+    x = wl.tokens(M, wl.LING.hidden, seed=6_100_000, device=DEV)
+    layer.set_router_bias(wl.zipf_router_bias(E))
+    tw = torch.empty((M, k), dtype=torch.float32, device=DEV)
+    _, idx = layer(x, topk_w=tw)
+    r = layer.read_routing(M)
+    ref = oracle.moe_forward(bits(x), host["wr"], host["wgu"], host["wd"], k,
+                             bias=wl.zipf_router_bias(E).numpy(), **variant)
+    same = np.all(idx.cpu().numpy() == ref["idx"], axis=1)
+    assert np.allclose(tw.cpu().numpy()[same], ref["w"][same], rtol=1e-5, atol=1e-7)
+    pw = r["pair_w"]
+    assert np.allclose(pw[:M * k], 2.5 * tw.cpu().numpy().ravel(), rtol=1e-6)
+    assert np.all(pw[M * k:] == 1.0)
+    shared_groups = r["grp_expert"] == E
+    assert shared_groups.sum() == 1 and r["grp_cnt"][shared_groups][0] == M
+    assert sorted(r["pair_list"].tolist()) == list(range(M * (k + 1)))
+    layer.set_router_bias(None)

@@ -26,6 +26,9 @@ struct LayerArgs {
   uint32_t d_tile;                // 8 rows x I x 2 bytes
   uint32_t ring_bytes;            // gu_stages*gu_tile + the reduction area
   int trace;                      // record phase timestamps
+  int shared;                     // 1: expert E is a shared expert every token passes (weight 1)
+  float routed_scale;             // factor on every routed weight
+  int sel_only;                   // 1: the bias picks the experts, unbiased logits weigh them
   Workspace ws;
 };
 

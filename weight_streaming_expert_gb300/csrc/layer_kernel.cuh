@@ -174,7 +174,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   if (tid == 0) stamp(a, 19);  // CTA started
   const int S = a.gu_stages;
   const int NSL = kConsumerWarps, SD = a.d_stages;  // slabs per down super tile, down slots
-  const int NP = a.M * a.K;
+  const int MK = a.M * a.K;                     // routed pairs (token * K + slot)
+  const int NP = MK + (a.shared ? a.M : 0);     // + the shared expert's pairs MK + token
+  const int EA = a.E + (a.shared ? 1 : 0);      // buckets: routed experts + the shared one
   const uint32_t sb = smem_u32(smem);
   int* stage_tile = reinterpret_cast<int*>(smem + kOffTile);
   int* dstage_tile = reinterpret_cast<int*>(smem + kOffDTile);
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   uint8_t* ring = smem + kRingOff;
   const uint32_t ring_u32 = sb + kRingOff;
   float4* red = reinterpret_cast<float4*>(ring + (size_t)S * a.gu_tile);
-  const SmemRouting rt = routing_carve(ring + a.ring_bytes, NP, a.E);
+  const SmemRouting rt = routing_carve(ring + a.ring_bytes, NP, EA);
   auto full = [&](int s) { return sb + kOffFull + 8u * s; };
   auto empty = [&](int s) { return sb + kOffEmpty + 8u * s; };
   auto ready = [&](int s) { return sb + kOffReady + 8u * s; };
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     }
     fence_mbar_init();
   }
-  for (int e = tid; e < a.E; e += kExpertThreads) rt.mask[e] = 0ull;
+  for (int e = tid; e < EA; e += kExpertThreads) rt.mask[e] = 0ull;
   for (int p = tid; p < NP; p += kExpertThreads) rt.pair_list[p] = 0;
   if (tid < 2) rt.scal[tid] = 0;
 
@@ -261,12 +263,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   // ---- 3. top-k of every token, compaction (every CTA, shared memory only)
   for (int m = warp; m < a.M; m += kExpertThreads / 32) {
     const float w = topk_dispatch(a.ws.part + (size_t)m * a.E, plane, a.ks, a.bias, a.E, a.K, lane,
-                                  a.ws.status, rt.s_e + m * a.K);
+                                  a.ws.status, rt.s_e + m * a.K, a.sel_only != 0);
     __syncwarp();
     if (lane < a.K) {
       const int p = m * a.K + lane;
       const int idx = rt.s_e[p];
-      rt.s_w[p] = w;
+      rt.s_w[p] = w * a.routed_scale;  // the combine's weight; topk_w is unscaled
       atomicOr(&rt.mask[idx], 1ull << m);
       if (blockIdx.x == 0) {
         a.topk_idx[p] = idx;
@@ -274,13 +276,19 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       }
     }
   }
+  if (a.shared && tid < a.M) {  // every token's pair with the shared expert, weight 1
+    const int p = MK + tid;
+    rt.s_e[p] = a.E;
+    rt.s_w[p] = 1.0f;
+    atomicOr(&rt.mask[a.E], 1ull << tid);
+  }
   __syncthreads();
   if (tid == 0) stamp(a, 12);
   // the reduction area is free until the gate/up loop: scratch for the
   // pair-axis compaction
   const int n_groups = a.M <= kGroupTokens
-                           ? compact_pairs(rt, NP, a.K, reinterpret_cast<int*>(red), tid, kExpertThreads)
-                           : (compact_masks(rt, a.M, a.K, a.E), rt.scal[0]);
+                           ? compact_pairs(rt, NP, a.K, MK, reinterpret_cast<int*>(red), tid, kExpertThreads)
+                           : (compact_masks(rt, NP, a.K, MK, EA), rt.scal[0]);
   if (tid == 0) stamp(a, 13);
   if (blockIdx.x == 0) {  // a copy for inspection (moe_read_routing); nothing reads it back
     for (int i = tid; i < NP; i += kExpertThreads) {
@@ -556,8 +564,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         // rows beyond the group's count repeat its first token, never stored
         start = rt.grp_start[g];
         cnt = rt.grp_cnt[g];
-        const int tok0 = rt.pair_list[start + (g4 < cnt ? g4 : 0)] / a.K;
-        const int tok1 = rt.pair_list[start + (g4 + 8 < cnt ? g4 + 8 : 0)] / a.K;
+        const int tok0 = pair_token(rt.pair_list[start + (g4 < cnt ? g4 : 0)], a.K, MK);
+        const int tok1 = pair_token(rt.pair_list[start + (g4 + 8 < cnt ? g4 + 8 : 0)], a.K, MK);
         const uint4* x0 = reinterpret_cast<const uint4*>(a.x + (size_t)tok0 * a.H) + t4;
         const uint4* x1 = reinterpret_cast<const uint4*>(a.x + (size_t)tok1 * a.H) + t4;
 #pragma unroll
@@ -716,6 +724,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int m = (it % per) / kDownTileRows;
     const int r = sl * kDownTileRows + (it % kDownTileRows);
     const float* yr = a.ws.y + (size_t)m * a.K * a.H + r;
+    const float vs = a.shared ? __ldcg(a.ws.y + (size_t)(MK + m) * a.H + r) : 0.f;  // the shared slot
     float sum = 0.f;
     for (int k0 = 0; k0 < a.K; k0 += 8) {  // 8 loads in flight, summed in slot order
       float v[8];
@@ -725,6 +734,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       for (int i = 0; i < 8; ++i)
         if (k0 + i < a.K) sum += v[i];
     }
+    if (a.shared) sum += vs;  // the shared slot, last
     a.out[(size_t)m * a.H + r] = __float2bfloat16_rn(sum);
   }
   if (tid == 0) stamp(a, 8);

@@ -67,6 +67,11 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct moe_layer {
   int H = 0, E = 0, K = 0, I = 0;
+  int shared = 0;           // 1: expert E (packed after the routed ones) is a shared expert
+  float routed_scale = 1.0f;
+  int sel_only = 0;         // the router bias picks the experts only
+  int kp() const { return K + shared; }  // pairs per token
+  int ea() const { return E + shared; }  // packed experts
   int dev = 0, n_sms = 0;
   __nv_bfloat16* w_router = nullptr;
   uint8_t* w_gu = nullptr;  // packed gate/up tiles
@@ -132,6 +137,9 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   la.d_tile = h->tile_d;
   la.ring_bytes = h->ring_bytes;
   la.trace = trace ? 1 : 0;
+  la.shared = h->shared;
+  la.routed_scale = h->routed_scale;
+  la.sel_only = h->sel_only;
   la.ws = h->ws;
 
   cudaLaunchAttribute attr[1];
@@ -143,7 +151,7 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   c.numAttrs = pdl ? 1 : 0;
   c.gridDim = dim3(h->n_sms);
   c.blockDim = dim3(kExpertThreads);
-  c.dynamicSmemBytes = layer_smem_bytes(h->ring_bytes, M * h->K, h->E);
+  c.dynamicSmemBytes = layer_smem_bytes(h->ring_bytes, M * h->kp(), h->ea());
 
   cudaError_t e;
   unsigned ev_flags = cudaEventRecordDefault;
@@ -182,6 +190,11 @@ const char* moe_last_error(void) { return g_last_error.c_str(); }
 
 moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const void* w_router,
                         const void* w_gate_up, const void* w_down) {
+  return moe_create_ex(hidden, n_experts, topk, inter, w_router, w_gate_up, w_down, nullptr);
+}
+
+moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const void* w_router,
+                           const void* w_gate_up, const void* w_down, const moe_layer_opts_t* opts) {
   g_last_error.clear();
   // ---- argument checks (no CUDA call before these pass) ----
   if (hidden <= 0 || hidden % 256 != 0 || !layer_kernel_for(hidden / 256)) {
@@ -208,6 +221,16 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
     set_err("weight pointers must be 16-byte aligned");
     return nullptr;
   }
+  const moe_layer_opts_t o = opts ? *opts : moe_layer_opts_t{};
+  if ((o.w_shared_gate_up == nullptr) != (o.w_shared_down == nullptr)) {
+    set_err("shared expert: give both w_shared_gate_up and w_shared_down, or neither");
+    return nullptr;
+  }
+  if (o.w_shared_gate_up && (!aligned16(o.w_shared_gate_up) || !aligned16(o.w_shared_down))) {
+    set_err("shared expert weight pointers must be 16-byte aligned");
+    return nullptr;
+  }
+  const int shared = o.w_shared_gate_up ? 1 : 0;
 
   // ---- device ----
   int dev = 0;
@@ -227,6 +250,9 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
 
   moe_layer* h = new moe_layer;
   h->H = hidden; h->E = n_experts; h->K = topk; h->I = inter;
+  h->shared = shared;
+  h->routed_scale = o.routed_scale > 0.f ? o.routed_scale : 1.0f;
+  h->sel_only = o.bias_selection_only ? 1 : 0;
   h->dev = dev;
   h->n_sms = prop.multiProcessorCount;
   h->kernel = layer_kernel_for(hidden / 256);
@@ -240,8 +266,8 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   // (one CTA per SM; deep rings keep enough bytes in flight to cover the
   // loaded HBM latency).
   const size_t optin = prop.sharedMemPerBlockOptin;
-  const int np_max = kMaxTokens * topk;
-  const size_t fixed = layer_smem_bytes(0, np_max, n_experts);
+  const int np_max = kMaxTokens * h->kp();
+  const size_t fixed = layer_smem_bytes(0, np_max, h->ea());
   const size_t avail = optin > fixed ? optin - fixed : 0;
   const size_t red = layer_reduction_bytes();
   h->s_gu = avail > red ? (int)std::min<size_t>(kMaxGateUpStages, (avail - red) / h->tile_gu) : 0;
@@ -255,11 +281,12 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
     free_layer(h);
     return nullptr;
   }
-  h->smem_max = layer_smem_bytes(h->ring_bytes, np_max, n_experts);
+  h->smem_max = layer_smem_bytes(h->ring_bytes, np_max, h->ea());
 
   AllocCounter ac;
   const size_t E = n_experts, H = hidden, I = inter;
-  const size_t b_router = E * H * 2, b_gu = E * 2 * I * H * 2, b_d = E * H * I * 2;
+  const size_t EA = (size_t)h->ea();  // routed experts, then the shared one
+  const size_t b_router = E * H * 2, b_gu = EA * 2 * I * H * 2, b_d = EA * H * I * 2;
   h->weight_bytes = b_router + b_gu + b_d;
   if (ac.alloc((void**)&h->w_router, b_router) != cudaSuccess ||
       ac.alloc((void**)&h->w_gu, b_gu) != cudaSuccess ||
@@ -271,7 +298,7 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
   }
 
   // workspace carve-up
-  const size_t np = (size_t)kMaxTokens * topk;
+  const size_t np = (size_t)kMaxTokens * h->kp();
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
   const size_t o_status = take(4), o_diag = take(32), o_sync = take(kSyncWords * 4);
@@ -319,6 +346,12 @@ moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const vo
                  n_experts, inter, hidden, s);
     pack_down(static_cast<const __nv_bfloat16*>(w_down), reinterpret_cast<__nv_bfloat16*>(h->w_d),
               n_experts, hidden, inter, s);
+    if (shared) {  // packed as expert index n_experts
+      pack_gate_up(static_cast<const __nv_bfloat16*>(o.w_shared_gate_up),
+                   reinterpret_cast<__nv_bfloat16*>(h->w_gu) + E * 2 * I * H, 1, inter, hidden, s);
+      pack_down(static_cast<const __nv_bfloat16*>(o.w_shared_down),
+                reinterpret_cast<__nv_bfloat16*>(h->w_d) + E * H * I, 1, hidden, inter, s);
+    }
     ok = cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
   }
   if (!ok) {
@@ -464,6 +497,9 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
   o->kernels_per_forward = 1;
   o->router_split = h->ks;
   o->smem_bytes = h->smem_max;
+  o->shared_expert = h->shared;
+  o->routed_scale = h->routed_scale;
+  o->bias_selection_only = h->sel_only;
   return MOE_OK;
 }
 
@@ -479,7 +515,7 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active, int32_
       (e = cudaMemcpy(n_active, h->ws.n_active, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "routing read");
   const int ng = *n_groups < cap ? *n_groups : cap;
-  const size_t np = (size_t)M * h->K;
+  const size_t np = (size_t)M * h->kp();
   if (ng > 0 && grp_expert && (e = cudaMemcpy(grp_expert, h->ws.grp_expert, ng * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "routing read");
   if (ng > 0 && grp_start && (e = cudaMemcpy(grp_start, h->ws.grp_start, ng * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)

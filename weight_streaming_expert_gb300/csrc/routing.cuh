@@ -196,11 +196,12 @@ __device__ __forceinline__ void top2_below(const uint32_t (&key)[VPL], uint32_t 
 // ks planes `plane` floats apart), summed in plane order, plus the bias.
 // Lane j < K writes slot j's expert id to idx_out[j] (the caller reads them
 // after a __syncwarp) and returns slot j's renormalised weight; the other
-// lanes return 0.
+// lanes return 0.  sel_only: the bias picks the experts only, the weights
+// come from the unbiased logits (re-read for the k chosen experts).
 template <int VPL>
 __device__ __forceinline__ float topk_token(const float* __restrict__ lg, size_t plane, int ks,
                                             const float* __restrict__ bias, int E, int K, int lane,
-                                            int* status, int* idx_out) {
+                                            int* status, int* idx_out, bool sel_only) {
   // planes 0 and 1 and the bias in one round trip; further planes one each;
   // the sum order is plane 0, 1, ..., then the bias
   float lv[VPL], l1[VPL], bv_[VPL];
@@ -262,20 +263,31 @@ __device__ __forceinline__ float topk_token(const float* __restrict__ lg, size_t
   }
   // weights: exp(l_j - l_0), normalised by a fixed butterfly sum over the
   // lanes that hold one (lanes >= K add 0)
-  const float ex = lane < K ? expf(key_value(my_key) - key_value(top0)) : 0.f;
+  float my_val = key_value(my_key), ref_val = key_value(top0);
+  if (sel_only && bias) {  // the unbiased logits of the chosen, summed as above
+    float l = 0.f;
+    if (lane < K) {
+      l = __ldcg(lg + my_win);
+      for (int c = 1; c < ks; ++c) l += __ldcg(lg + (size_t)c * plane + my_win);
+    }
+    my_val = l;
+    ref_val = key_value(__reduce_max_sync(0xffffffffu, lane < K ? ordered_key(l) : 0u));
+  }
+  const float ex = lane < K ? expf(my_val - ref_val) : 0.f;
   float s = ex;
   for (int o = 1; o < K; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return lane < K ? __fdividef(ex, s) : 0.f;
 }
 
 __device__ __forceinline__ float topk_dispatch(const float* lg, size_t plane, int ks, const float* bias,
-                                               int E, int K, int lane, int* status, int* idx_out) {
-  if (E <= 32) return topk_token<1>(lg, plane, ks, bias, E, K, lane, status, idx_out);
-  if (E <= 64) return topk_token<2>(lg, plane, ks, bias, E, K, lane, status, idx_out);
-  if (E <= 128) return topk_token<4>(lg, plane, ks, bias, E, K, lane, status, idx_out);
-  if (E <= 256) return topk_token<8>(lg, plane, ks, bias, E, K, lane, status, idx_out);
-  if (E <= 512) return topk_token<16>(lg, plane, ks, bias, E, K, lane, status, idx_out);
-  return topk_token<32>(lg, plane, ks, bias, E, K, lane, status, idx_out);
+                                               int E, int K, int lane, int* status, int* idx_out,
+                                               bool sel_only = false) {
+  if (E <= 32) return topk_token<1>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 64) return topk_token<2>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 128) return topk_token<4>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 256) return topk_token<8>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 512) return topk_token<16>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
+  return topk_token<32>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
 }
 
 // ------------------------------------------------------- compaction ----
@@ -313,13 +325,16 @@ __device__ __forceinline__ SmemRouting routing_carve(uint8_t* base, int NP, int 
   return r;
 }
 
+// Token of pair p: routed pairs p = token * K + slot come first (MK = M * K
+// of them), then the shared expert's pairs MK + token.
+__device__ __forceinline__ int pair_token(int p, int K, int MK) { return p < MK ? p / K : p - MK; }
+
 // Cooperative over the CTA; mask[] and s_e[] complete and visible (a
 // __syncthreads() before).  Bucket sizes and group counts by a block-wide
 // scan over the experts; every pair then takes its place independently.
-// Ends with a __syncthreads().
-__device__ inline void compact_masks(const SmemRouting& r, int M, int K, int E) {
+// NP pairs (MK routed, see pair_token).  Ends with a __syncthreads().
+__device__ inline void compact_masks(const SmemRouting& r, int NP, int K, int MK, int E) {
   const int tid = threadIdx.x, nt = blockDim.x;
-  const int NP = M * K;
   // (pairs << 16) + groups share one int (both <= 2048, no carry)
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   int* s_wt = r.scal + 8;
@@ -387,7 +402,7 @@ __device__ inline void compact_masks(const SmemRouting& r, int M, int K, int E) 
   }
   __syncthreads();
   for (int p = tid; p < NP; p += nt) {
-    const int e = r.s_e[p], m = p / K;
+    const int e = r.s_e[p], m = pair_token(p, K, MK);
     const int rank = __popcll(r.mask[e] & ((1ull << m) - 1ull));
     r.pair_list[r.s_off[e] + rank] = p;
   }
@@ -403,12 +418,13 @@ __device__ inline void compact_masks(const SmemRouting& r, int M, int K, int E) 
 // and the pair of e with the lowest token opens e's group, numbered by the
 // group openers with a smaller expert.  Two short loops over the NP pairs
 // per thread (the code stays small: it runs once per call, cold), no scan.
-// ekey: NP ints of scratch.  Cooperative over threads t, t + nt, ...; mask[]
+// NP pairs (MK routed, see pair_token).  ekey: NP ints of scratch.
+// Cooperative over threads t, t + nt, ...; mask[]
 // and s_e[] complete and visible (a barrier before); scal[0] zero.  Ends
 // with a __syncthreads(); returns the group count.
-__device__ inline int compact_pairs(const SmemRouting& r, int NP, int K, int* ekey, int t, int nt) {
+__device__ inline int compact_pairs(const SmemRouting& r, int NP, int K, int MK, int* ekey, int t, int nt) {
   for (int p = t; p < NP; p += nt) {
-    const int e = r.s_e[p], m = p / K;
+    const int e = r.s_e[p], m = pair_token(p, K, MK);
     ekey[p] = (e << 1) | ((r.mask[e] & ((1ull << m) - 1ull)) == 0ull ? 1 : 0);
   }
   __syncthreads();

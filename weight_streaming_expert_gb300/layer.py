@@ -29,7 +29,8 @@ class MoELayer:
       w_router  [E, H]     w_gate_up [E, 2I, H] (gate rows first)   w_down [E, H, I]
     """
 
-    def __init__(self, w_router, w_gate_up, w_down, topk: int):
+    def __init__(self, w_router, w_gate_up, w_down, topk: int, shared_gate_up=None, shared_down=None,
+                 routed_scale: float = 1.0, bias_selection_only: bool = False):
         E, H = w_router.shape
         I = w_down.shape[2]
         for t in (w_router, w_gate_up, w_down):
@@ -37,11 +38,20 @@ class MoELayer:
                 raise ValueError("weights must be contiguous bf16 CUDA tensors")
         if tuple(w_gate_up.shape) != (E, 2 * I, H) or tuple(w_down.shape) != (E, H, I):
             raise ValueError("weight shapes must be [E,H], [E,2I,H], [E,H,I]")
+        if (shared_gate_up is None) != (shared_down is None):
+            raise ValueError("give both shared_gate_up and shared_down, or neither")
+        if shared_gate_up is not None and (tuple(shared_gate_up.shape) != (2 * I, H)
+                                           or tuple(shared_down.shape) != (H, I)):
+            raise ValueError("shared expert shapes must be [2I,H] and [H,I]")
         self.hidden, self.n_experts, self.topk, self.inter = H, E, topk, I
+        self.shared = shared_gate_up is not None
         self.device = w_router.device
         L = N.lib()
+        opts = N.moe_layer_opts_t(None if shared_gate_up is None else shared_gate_up.data_ptr(),
+                                  None if shared_down is None else shared_down.data_ptr(),
+                                  float(routed_scale), 1 if bias_selection_only else 0)
         with torch.cuda.device(self.device):
-            h = L.moe_create(H, E, topk, I, _ptr(w_router), _ptr(w_gate_up), _ptr(w_down))
+            h = L.moe_create_ex(H, E, topk, I, _ptr(w_router), _ptr(w_gate_up), _ptr(w_down), ctypes.byref(opts))
         if not h:
             raise N.MoEError("moe_create", N.MOE_ERR_INVALID_ARG, N.last_error())
         self._h = ctypes.c_void_p(h)
@@ -110,7 +120,8 @@ class MoELayer:
     def read_routing(self, M: int):
         """Last call's on-device compaction as numpy arrays (synchronises)."""
         import numpy as np
-        cap = max(1, M * self.topk)
+        np_ = M * (self.topk + (1 if self.shared else 0))  # pairs, the shared expert's last
+        cap = max(1, np_)
         ng, na = ctypes.c_int(), ctypes.c_int()
         ge = np.zeros(cap, np.int32)
         gs = np.zeros(cap, np.int32)
@@ -125,7 +136,7 @@ class MoELayer:
         N.check("moe_read_routing", rc)
         n = ng.value
         return dict(n_groups=n, n_active=na.value, grp_expert=ge[:n], grp_start=gs[:n], grp_cnt=gc[:n],
-                    pair_list=pl[:M * self.topk], pair_w=pw[:M * self.topk])
+                    pair_list=pl[:np_], pair_w=pw[:np_])
 
     def close(self):
         if getattr(self, "_h", None):

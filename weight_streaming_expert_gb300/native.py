@@ -40,7 +40,13 @@ class moe_info_t(ctypes.Structure):
                 ("gateup_tile_bytes", ctypes.c_int), ("down_tile_bytes", ctypes.c_int),
                 ("weight_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
                 ("kernels_per_forward", ctypes.c_int), ("router_split", ctypes.c_int),
-                ("smem_bytes", ctypes.c_size_t)]
+                ("smem_bytes", ctypes.c_size_t), ("shared_expert", ctypes.c_int),
+                ("routed_scale", ctypes.c_float), ("bias_selection_only", ctypes.c_int)]
+
+
+class moe_layer_opts_t(ctypes.Structure):
+    _fields_ = [("w_shared_gate_up", ctypes.c_void_p), ("w_shared_down", ctypes.c_void_p),
+                ("routed_scale", ctypes.c_float), ("bias_selection_only", ctypes.c_int)]
 
 
 class MoEError(RuntimeError):
@@ -71,6 +77,8 @@ def lib(build_if_missing: bool = True):
         ip = ctypes.POINTER(ctypes.c_int)
         L.moe_create.argtypes = [ci, ci, ci, ci, vp, vp, vp]
         L.moe_create.restype = vp
+        L.moe_create_ex.argtypes = [ci, ci, ci, ci, vp, vp, vp, ctypes.POINTER(moe_layer_opts_t)]
+        L.moe_create_ex.restype = vp
         L.moe_forward.argtypes = [vp, vp, vp, vp, ci, vp]
         L.moe_forward.restype = ci
         L.moe_forward_ex.argtypes = [vp, vp, vp, vp, vp, ci, vp, cu]
