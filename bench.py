@@ -63,7 +63,7 @@ def source_hash(paths):
 
 LAYER_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
                  for f in ("layer_kernel.cuh", "routing.cuh", "common.cuh", "kernels.cuh",
-                           "layer_kernel_a.cu", "layer_kernel_b.cu")]
+                           "layer_kernel_a.cu", "layer_kernel_b.cu", "layer_kernel_c.cu", "layer_kernel_d.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "layer_traffic.json")
 
 

@@ -33,9 +33,11 @@ struct LayerArgs {
 };
 
 // The layer kernel: grid = #SMs x kExpertThreads, dynamic shared memory
-// layer_smem_bytes(ring_bytes, M*K, E).  KPW = H/256.
+// layer_smem_bytes(ring_bytes, NP, buckets).  KPW = H/256.
 using LayerKernel = void (*)(LayerArgs);
-LayerKernel layer_kernel_for(int kpw);
+// variant: the instance that handles the layer variants (nullptr: no such
+// kpw).
+LayerKernel layer_kernel_for(int kpw, bool variant);
 size_t layer_smem_bytes(uint32_t ring_bytes, int NP, int E);
 // Bytes of the reduction area that follows the gate/up stages.
 uint32_t layer_reduction_bytes();

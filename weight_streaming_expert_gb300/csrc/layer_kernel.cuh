@@ -166,7 +166,10 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g));
 
 }  // namespace layer_detail
 
-template <int KPW>  // H / 256: 32-wide k chunks per warp in the gate/up GEMV
+// KPW = H / 256: 32-wide k chunks per warp in the gate/up GEMV.  VARIANT:
+// the instance that handles the layer variants (shared expert, routed scale,
+// selection-only bias); the plain instance compiles none of their code.
+template <int KPW, bool VARIANT>
 __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs a) {
   using namespace layer_detail;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -175,8 +178,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   const int S = a.gu_stages;
   const int NSL = kConsumerWarps, SD = a.d_stages;  // slabs per down super tile, down slots
   const int MK = a.M * a.K;                     // routed pairs (token * K + slot)
-  const int NP = MK + (a.shared ? a.M : 0);     // + the shared expert's pairs MK + token
-  const int EA = a.E + (a.shared ? 1 : 0);      // buckets: routed experts + the shared one
+  const bool shared = VARIANT && a.shared;
+  const int NP = MK + (shared ? a.M : 0);       // + the shared expert's pairs MK + token
+  const int EA = a.E + (shared ? 1 : 0);        // buckets: routed experts + the shared one
   const uint32_t sb = smem_u32(smem);
   int* stage_tile = reinterpret_cast<int*>(smem + kOffTile);
   int* dstage_tile = reinterpret_cast<int*>(smem + kOffDTile);
@@ -263,12 +267,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   // ---- 3. top-k of every token, compaction (every CTA, shared memory only)
   for (int m = warp; m < a.M; m += kExpertThreads / 32) {
     const float w = topk_dispatch(a.ws.part + (size_t)m * a.E, plane, a.ks, a.bias, a.E, a.K, lane,
-                                  a.ws.status, rt.s_e + m * a.K, a.sel_only != 0);
+                                  a.ws.status, rt.s_e + m * a.K, VARIANT && a.sel_only != 0);
     __syncwarp();
     if (lane < a.K) {
       const int p = m * a.K + lane;
       const int idx = rt.s_e[p];
-      rt.s_w[p] = w * a.routed_scale;  // the combine's weight; topk_w is unscaled
+      rt.s_w[p] = VARIANT ? w * a.routed_scale : w;  // the combine's weight; topk_w is unscaled
       atomicOr(&rt.mask[idx], 1ull << m);
       if (blockIdx.x == 0) {
         a.topk_idx[p] = idx;
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       }
     }
   }
-  if (a.shared && tid < a.M) {  // every token's pair with the shared expert, weight 1
+  if (shared && tid < a.M) {  // every token's pair with the shared expert, weight 1
     const int p = MK + tid;
     rt.s_e[p] = a.E;
     rt.s_w[p] = 1.0f;
@@ -564,8 +568,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         // rows beyond the group's count repeat its first token, never stored
         start = rt.grp_start[g];
         cnt = rt.grp_cnt[g];
-        const int tok0 = pair_token(rt.pair_list[start + (g4 < cnt ? g4 : 0)], a.K, MK);
-        const int tok1 = pair_token(rt.pair_list[start + (g4 + 8 < cnt ? g4 + 8 : 0)], a.K, MK);
+        const int p0 = rt.pair_list[start + (g4 < cnt ? g4 : 0)];
+        const int p1 = rt.pair_list[start + (g4 + 8 < cnt ? g4 + 8 : 0)];
+        const int tok0 = VARIANT ? pair_token(p0, a.K, MK) : p0 / a.K;
+        const int tok1 = VARIANT ? pair_token(p1, a.K, MK) : p1 / a.K;
         const uint4* x0 = reinterpret_cast<const uint4*>(a.x + (size_t)tok0 * a.H) + t4;
         const uint4* x1 = reinterpret_cast<const uint4*>(a.x + (size_t)tok1 * a.H) + t4;
 #pragma unroll
@@ -724,7 +730,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int m = (it % per) / kDownTileRows;
     const int r = sl * kDownTileRows + (it % kDownTileRows);
     const float* yr = a.ws.y + (size_t)m * a.K * a.H + r;
-    const float vs = a.shared ? __ldcg(a.ws.y + (size_t)(MK + m) * a.H + r) : 0.f;  // the shared slot
+    const float vs = shared ? __ldcg(a.ws.y + (size_t)(MK + m) * a.H + r) : 0.f;  // the shared slot
     float sum = 0.f;
     for (int k0 = 0; k0 < a.K; k0 += 8) {  // 8 loads in flight, summed in slot order
       float v[8];
@@ -734,7 +740,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       for (int i = 0; i < 8; ++i)
         if (k0 + i < a.K) sum += v[i];
     }
-    if (a.shared) sum += vs;  // the shared slot, last
+    if (shared) sum += vs;  // the shared slot, last
     a.out[(size_t)m * a.H + r] = __float2bfloat16_rn(sum);
   }
   if (tid == 0) stamp(a, 8);

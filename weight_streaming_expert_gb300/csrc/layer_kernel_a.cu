@@ -1,15 +1,15 @@
-// layer_kernel_a.cu -- layer kernel instances for hidden = 256 x {1,2,4,5}
-// (split from layer_kernel_b.cu so the two compile in parallel).
+// layer_kernel_a.cu -- layer kernel instances for hidden = 256 x {1,2,4,5}, plain
+// (four translation units so that the instances compile in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {
 
-LayerKernel layer_kernel_small(int kpw) {
+LayerKernel layer_kernel_plain_small(int kpw) {
   switch (kpw) {
-    case 1: return moe_layer_kernel<1>;
-    case 2: return moe_layer_kernel<2>;
-    case 4: return moe_layer_kernel<4>;
-    case 5: return moe_layer_kernel<5>;
+    case 1: return moe_layer_kernel<1, false>;
+    case 2: return moe_layer_kernel<2, false>;
+    case 4: return moe_layer_kernel<4, false>;
+    case 5: return moe_layer_kernel<5, false>;
     default: return nullptr;
   }
 }

@@ -1,0 +1,17 @@
+// layer_kernel_d.cu -- layer kernel instances for hidden = 256 x {8,10,12,16}, layer variants
+// (four translation units so that the instances compile in parallel).
+#include "layer_kernel.cuh"
+
+namespace wse {
+
+LayerKernel layer_kernel_variant_large(int kpw) {
+  switch (kpw) {
+    case 8: return moe_layer_kernel<8, true>;
+    case 10: return moe_layer_kernel<10, true>;
+    case 12: return moe_layer_kernel<12, true>;
+    case 16: return moe_layer_kernel<16, true>;
+    default: return nullptr;
+  }
+}
+
+}  // namespace wse

@@ -197,7 +197,7 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
                            const void* w_gate_up, const void* w_down, const moe_layer_opts_t* opts) {
   g_last_error.clear();
   // ---- argument checks (no CUDA call before these pass) ----
-  if (hidden <= 0 || hidden % 256 != 0 || !layer_kernel_for(hidden / 256)) {
+  if (hidden <= 0 || hidden % 256 != 0 || !layer_kernel_for(hidden / 256, false)) {
     set_err("hidden = %d unsupported: need a multiple of 256 with hidden/256 in {1,2,4,5,8,10,12,16}",
             hidden);
     return nullptr;
@@ -243,7 +243,8 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
     return nullptr;
   }
   cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, layer_kernel_for(hidden / 256))) != cudaSuccess) {
+  const bool variant = o.w_shared_gate_up || o.bias_selection_only || (o.routed_scale > 0.f && o.routed_scale != 1.0f);
+  if ((e = cudaFuncGetAttributes(&fa, layer_kernel_for(hidden / 256, variant))) != cudaSuccess) {
     cuda_fail(e, "kernel image");
     return nullptr;
   }
@@ -255,7 +256,7 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
   h->sel_only = o.bias_selection_only ? 1 : 0;
   h->dev = dev;
   h->n_sms = prop.multiProcessorCount;
-  h->kernel = layer_kernel_for(hidden / 256);
+  h->kernel = layer_kernel_for(hidden / 256, variant);
   h->tile_gu = (uint32_t)(kGateUpTileRows * hidden * 2);
   h->tile_d = (uint32_t)(kDownTileRows * inter * 2);
   h->ks = gemv_split(hidden, n_experts, h->n_sms);
