@@ -39,6 +39,7 @@
 // rounding sequence is the one written here on every host).
 
 #include <cmath>
+#include <limits>
 #include <cstdint>
 #include <cstring>
 #include <vector>
@@ -204,6 +205,107 @@ int oracle_expert_down(int H, int I, const uint16_t* h_row,
       acc = acc + oracle_bf16_to_f32(h_row[r]) * oracle_bf16_to_f32(wd[r]);
     y[j] = acc;
   }
+  return 0;
+}
+
+// --------------------------------------------------------------- fp8 ----
+// Expert weights in fp8 (the post: "once fp8 weights shrink the fixed
+// base"): OCP FP8 E4M3 codes with one fp32 scale per output row; the
+// dequantized matrix is diag(scale) * decode(codes).
+
+// E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+// infinities, S.1111.111 is NaN.  Exact value as fp32.
+float oracle_e4m3_to_f32(uint8_t v) {
+  const int s = v >> 7, e = (v >> 3) & 15, m = v & 7;
+  float mag;
+  if (e == 15 && m == 7)
+    mag = std::numeric_limits<float>::quiet_NaN();
+  else if (e == 0)
+    mag = std::ldexp((float)m, -9);  // subnormal: (m / 8) * 2^-6
+  else
+    mag = std::ldexp(1.0f + (float)m / 8.0f, e - 7);
+  return s ? -mag : mag;
+}
+
+// Gate/up of one token through one fp8 expert (codes [2I][H], scales [2I]):
+// g = s[r] * sum_h x[h] * q[r][h], u likewise with row I + r (the row scale
+// factored out of the fp32 sum); h = bf16(silu(g) * u).
+int oracle_expert_swiglu_fp8(int H, int I, const uint16_t* x_row, const uint8_t* q_gu_e,
+                             const float* s_gu_e, uint16_t* h_out) {
+  if (H <= 0 || I <= 0 || !x_row || !q_gu_e || !s_gu_e || !h_out) return 1;
+  for (int r = 0; r < I; ++r) {
+    float g = 0.0f, u = 0.0f;
+    const uint8_t* qg = q_gu_e + (size_t)r * H;
+    const uint8_t* qu = q_gu_e + (size_t)(I + r) * H;
+    for (int h = 0; h < H; ++h) {
+      float xv = oracle_bf16_to_f32(x_row[h]);
+      g = g + xv * oracle_e4m3_to_f32(qg[h]);
+      u = u + xv * oracle_e4m3_to_f32(qu[h]);
+    }
+    h_out[r] = oracle_swiglu_bf16(s_gu_e[r] * g, s_gu_e[I + r] * u);
+  }
+  return 0;
+}
+
+// Down projection of one activated row through one fp8 expert (codes
+// [H][I], scales [H]): y[j] = s[j] * sum_r h[r] * q[j][r].
+int oracle_expert_down_fp8(int H, int I, const uint16_t* h_row, const uint8_t* q_d_e, const float* s_d_e,
+                           float* y) {
+  if (H <= 0 || I <= 0 || !h_row || !q_d_e || !s_d_e || !y) return 1;
+  for (int j = 0; j < H; ++j) {
+    float acc = 0.0f;
+    const uint8_t* qd = q_d_e + (size_t)j * I;
+    for (int r = 0; r < I; ++r) acc = acc + oracle_bf16_to_f32(h_row[r]) * oracle_e4m3_to_f32(qd[r]);
+    y[j] = s_d_e[j] * acc;
+  }
+  return 0;
+}
+
+// The layer with fp8 expert weights (router bf16, routing and combine as
+// oracle_moe_forward): q_gate_up [E][2I][H] + s_gate_up [E][2I],
+// q_down [E][H][I] + s_down [E][H].  Outputs as oracle_moe_forward.
+int oracle_moe_forward_fp8(int M, int H, int E, int K, int I, const uint16_t* x, const uint16_t* w_router,
+                           const float* bias, const uint8_t* q_gate_up, const float* s_gate_up,
+                           const uint8_t* q_down, const float* s_down, const int32_t* idx_in,
+                           float* logits_out, int32_t* idx_out, float* w_out, float* acc_out, uint16_t* out) {
+  if (M < 0 || H <= 0 || E <= 0 || K <= 0 || K > E || I <= 0) return 1;
+  if (!x || !w_router || !q_gate_up || !s_gate_up || !q_down || !s_down || !out) return 1;
+  if (M == 0) return 0;
+  std::vector<float> logits((size_t)M * E);
+  std::vector<int32_t> idx((size_t)M * K);
+  std::vector<float> w((size_t)M * K);
+  if (oracle_router_logits(M, H, E, x, w_router, bias, logits.data())) return 1;
+  if (idx_in) {
+    for (int m = 0; m < M; ++m) {
+      for (int j = 0; j < K; ++j) idx[(size_t)m * K + j] = idx_in[(size_t)m * K + j];
+      if (oracle_weights_for_set(E, K, logits.data() + (size_t)m * E, idx.data() + (size_t)m * K,
+                                 w.data() + (size_t)m * K))
+        return 1;
+    }
+  } else {
+    oracle_topk_softmax(M, E, K, logits.data(), idx.data(), w.data());
+  }
+  std::vector<uint16_t> hrow(I);
+  std::vector<float> y(H), acc(H);
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* xr = x + (size_t)m * H;
+    for (int j = 0; j < H; ++j) acc[j] = 0.0f;
+    for (int s = 0; s < K; ++s) {
+      const int e = idx[(size_t)m * K + s];
+      oracle_expert_swiglu_fp8(H, I, xr, q_gate_up + (size_t)e * 2 * I * H, s_gate_up + (size_t)e * 2 * I,
+                               hrow.data());
+      oracle_expert_down_fp8(H, I, hrow.data(), q_down + (size_t)e * H * I, s_down + (size_t)e * H, y.data());
+      const float ws = w[(size_t)m * K + s];
+      for (int j = 0; j < H; ++j) acc[j] = acc[j] + ws * y[j];
+    }
+    for (int j = 0; j < H; ++j) {
+      if (acc_out) acc_out[(size_t)m * H + j] = acc[j];
+      out[(size_t)m * H + j] = oracle_f32_to_bf16(acc[j]);
+    }
+  }
+  if (logits_out) std::memcpy(logits_out, logits.data(), logits.size() * 4);
+  if (idx_out) std::memcpy(idx_out, idx.data(), idx.size() * 4);
+  if (w_out) std::memcpy(w_out, w.data(), w.size() * 4);
   return 0;
 }
 

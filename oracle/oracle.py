@@ -61,11 +61,16 @@ def load(path: str | None = None):
         lib.oracle_moe_forward.argtypes = [ci, ci, ci, ci, ci, u16p, u16p, f32p, u16p, u16p,
                                            i32p, f32p, i32p, f32p, f32p, u16p, u16p]
         lib.oracle_lm_head.argtypes = [ci, ci, ci, u16p, u16p, f32p]
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f32.restype = ctypes.c_float
+        lib.oracle_moe_forward_fp8.argtypes = [ci, ci, ci, ci, ci, u16p, u16p, f32p, u8p, f32p, u8p, f32p,
+                                               i32p, f32p, i32p, f32p, f32p, u16p]
         lib.oracle_moe_forward_ex.argtypes = [ci, ci, ci, ci, ci, u16p, u16p, f32p, ci, u16p, u16p, u16p, u16p,
                                               ctypes.c_float, i32p, f32p, i32p, f32p, f32p, u16p, u16p]
         for name in ("oracle_router_logits", "oracle_topk_softmax", "oracle_weights_for_set",
                      "oracle_expert_swiglu", "oracle_expert_down", "oracle_moe_forward", "oracle_lm_head",
-                     "oracle_moe_forward_ex"):
+                     "oracle_moe_forward_ex", "oracle_moe_forward_fp8"):
             getattr(lib, name).restype = ci
         if path is None:
             _lib = lib
@@ -201,3 +206,36 @@ class Oracle:
         if want_h:
             res["h"] = h
         return res
+
+    # fp8 expert weights ---------------------------------------------------
+    def e4m3_to_f32(self, code: int) -> float:
+        return float(self.lib.oracle_e4m3_to_f32(int(code)))
+
+    def moe_forward_fp8(self, x, w_router, q_gate_up, s_gate_up, q_down, s_down, k, bias=None, idx_in=None):
+        """The layer with fp8 (E4M3) expert weights and per-row fp32 scales:
+        q_gate_up u8 [E,2I,H], s_gate_up f32 [E,2I], q_down u8 [E,H,I],
+        s_down f32 [E,H].  Returns dict(out, acc, logits, idx, w)."""
+        x, w_router = _u16(x), _u16(w_router)
+        q_gate_up = np.ascontiguousarray(q_gate_up, np.uint8)
+        q_down = np.ascontiguousarray(q_down, np.uint8)
+        s_gate_up = np.ascontiguousarray(s_gate_up, np.float32)
+        s_down = np.ascontiguousarray(s_down, np.float32)
+        M, H = x.shape
+        E = w_router.shape[0]
+        I = q_down.shape[2]
+        assert q_gate_up.shape == (E, 2 * I, H) and s_gate_up.shape == (E, 2 * I)
+        assert q_down.shape == (E, H, I) and s_down.shape == (E, H)
+        logits = np.zeros((M, E), np.float32)
+        idx = np.zeros((M, k), np.int32)
+        w = np.zeros((M, k), np.float32)
+        acc = np.zeros((M, H), np.float32)
+        out = np.zeros((M, H), np.uint16)
+        b = None if bias is None else np.ascontiguousarray(bias, np.float32)
+        ii = None if idx_in is None else np.ascontiguousarray(idx_in, np.int32)
+        rc = self.lib.oracle_moe_forward_fp8(
+            M, H, E, k, I, _p(x, ctypes.c_uint16), _p(w_router, ctypes.c_uint16), _p(b, ctypes.c_float),
+            _p(q_gate_up, ctypes.c_uint8), _p(s_gate_up, ctypes.c_float), _p(q_down, ctypes.c_uint8),
+            _p(s_down, ctypes.c_float), _p(ii, ctypes.c_int32), _p(logits, ctypes.c_float),
+            _p(idx, ctypes.c_int32), _p(w, ctypes.c_float), _p(acc, ctypes.c_float), _p(out, ctypes.c_uint16))
+        assert rc == 0, "oracle rejected its arguments"
+        return dict(out=out, acc=acc, logits=logits, idx=idx, w=w)

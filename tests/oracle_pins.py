@@ -344,6 +344,65 @@ def pin_selection_only_bias(orc):
     assert not np.allclose(rb["w"], r["w"]), "the two bias modes must weigh differently"
 
 
+def pin_e4m3_decode(orc):
+    """Every E4M3 code against torch's float8_e4m3fn, plus hand values."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).float().numpy()
+    got = np.array([orc.e4m3_to_f32(c) for c in range(256)], np.float32)
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2, "NaN codes are S.1111.111 only"
+    assert np.array_equal(got[~nan], lib[~nan]), "E4M3 decode != torch"
+    for code, val in ((0x7E, 448.0), (0x38, 1.0), (0x01, 2.0 ** -9), (0xC6, -3.5), (0x08, 2.0 ** -6)):
+        assert orc.e4m3_to_f32(code) == val
+
+
+def _fp8_tiny(seed):
+    shape = wl.TINY
+    w_r, q_gu, s_gu, q_d, s_d = wl.fp8_expert_weights(shape, seed=seed)
+    x = wl.tokens(4, shape.hidden, seed=seed + 1)
+    return shape, _np(x), _np(w_r), q_gu.numpy(), s_gu.numpy(), q_d.numpy(), s_d.numpy()
+
+
+def pin_fp8_unit_scales_are_bf16(orc):
+    """With unit scales the fp8 layer is the bf16 layer on the decoded codes
+    (every E4M3 value is a bf16 value), bit for bit."""
+    shape, x, w_r, q_gu, _, q_d, _ = _fp8_tiny(31)
+    E, I, H = shape.n_experts, shape.inter, shape.hidden
+    one_gu, one_d = np.ones((E, 2 * I), np.float32), np.ones((E, H), np.float32)
+    f8 = orc.moe_forward_fp8(x, w_r, q_gu, one_gu, q_d, one_d, shape.topk)
+    dec = lambda q: bf16_round_torch(torch.from_numpy(q).view(torch.float8_e4m3fn).float().numpy())
+    bf = orc.moe_forward(x, w_r, dec(q_gu), dec(q_d), shape.topk)
+    assert np.array_equal(f8["idx"], bf["idx"])
+    assert np.array_equal(f8["acc"], bf["acc"]) and np.array_equal(f8["out"], bf["out"])
+
+
+def pin_fp8_dense(orc):
+    """Per-row scales against a float64 dense brute force on the dequantized
+    weights diag(scale) * decode(codes)."""
+    shape, x, w_r, q_gu, s_gu, q_d, s_d = _fp8_tiny(33)
+    I = shape.inter
+    f8 = orc.moe_forward_fp8(x, w_r, q_gu, s_gu, q_d, s_d, shape.topk)
+    dec = lambda q: torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy()
+    Wgu = dec(q_gu) * s_gu[:, :, None].astype(np.float64)
+    Wd = dec(q_d) * s_d[:, :, None].astype(np.float64)
+    X = f32_of_bits(x).astype(np.float64)
+    Wr = f32_of_bits(w_r).astype(np.float64)
+    logits = X @ Wr.T
+    G = np.einsum("eih,mh->mei", Wgu[:, :I, :], X)
+    U = np.einsum("eih,mh->mei", Wgu[:, I:, :], X)
+    hh = f32_of_bits(bf16_round_torch((silu64(G) * U).astype(np.float32))).astype(np.float64)
+    Y = np.einsum("ehi,mei->meh", Wd, hh)
+    M, E = X.shape[0], shape.n_experts
+    acc = np.zeros((M, shape.hidden))
+    for m in range(M):
+        order = np.lexsort((np.arange(E), -logits[m]))[:shape.topk]
+        assert np.array_equal(f8["idx"][m], order)
+        p = np.exp(logits[m][order] - logits[m][order].max())
+        acc[m] = (p / p.sum()) @ Y[m, order]
+    assert rel_l2(f8["acc"], acc) < 2e-3, "fp8 layer != dense brute force on dequantized weights"
+
+
 ALL_PINS = [pin_bf16_rounding, pin_router_logits, pin_topk_brute_force, pin_swiglu,
             pin_dense_bruteforce, pin_one_hot_router, pin_special_cases, pin_expert_permutation,
-            pin_lm_head, pin_shared_expert_and_scale, pin_selection_only_bias]
+            pin_lm_head, pin_shared_expert_and_scale, pin_selection_only_bias, pin_e4m3_decode,
+            pin_fp8_unit_scales_are_bf16, pin_fp8_dense]

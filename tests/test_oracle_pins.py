@@ -49,6 +49,11 @@ MUTANTS = {
                                   "for (int k = 0; k + 1 < H; ++k) acc"),
     "shared_expert_dropped": ("for (int j = 0; j < H; ++j) acc[j] = acc[j] + ys[j];", "(void)ys;"),
     "routed_scale_ignored": ("float ws = routed_scale * w[(size_t)m * K + s];", "float ws = w[(size_t)m * K + s];"),
+    "e4m3_bias_off_by_one": ("mag = std::ldexp(1.0f + (float)m / 8.0f, e - 7);",
+                             "mag = std::ldexp(1.0f + (float)m / 8.0f, e - 8);"),
+    "fp8_gate_scale_ignored": ("h_out[r] = oracle_swiglu_bf16(s_gu_e[r] * g, s_gu_e[I + r] * u);",
+                               "h_out[r] = oracle_swiglu_bf16(g, s_gu_e[I + r] * u);"),
+    "fp8_down_scale_shifted": ("y[j] = s_d_e[j] * acc;", "y[j] = s_d_e[(j + 1) % H] * acc;"),
     "selection_weights_from_biased_logits": ("const float* wlog = sel_only ? unbiased.data() : logits.data();",
                                              "const float* wlog = logits.data();"),
 }

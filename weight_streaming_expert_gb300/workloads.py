@@ -91,6 +91,37 @@ def lm_head_weight(vocab: int, hidden: int, seed: int, device="cpu", std: float 
     return w
 
 
+def fp8_rows(w: torch.Tensor):
+    """Per-row fp8 (E4M3) codes and fp32 scales of a weight [..., rows, cols]:
+    scale = max|row| / 448 (1 for an all-zero row), code = E4M3(w / scale)
+    rounded to nearest even by torch's conversion.  Returns (uint8 codes,
+    float32 scales [..., rows])."""
+    w = w.float()
+    amax = w.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (w / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q, scale.to(torch.float32)
+
+
+def fp8_expert_weights(shape: LayerShape, seed: int, device="cpu", std: float = WEIGHT_STD):
+    """(w_router bf16 [E,H], q_gate_up u8 [E,2I,H], s_gate_up f32 [E,2I],
+    q_down u8 [E,H,I], s_down f32 [E,H]): the router as layer_weights draws
+    it, the experts drawn in fp32 ~ N(0, std) and quantized per output row
+    (expert by expert on CUDA to bound temporaries)."""
+    g = _gen(seed, device)
+    E, H, I = shape.n_experts, shape.hidden, shape.inter
+    w_r = _randn_bf16((E, H), std, g, device)
+    q_gu = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=device)
+    s_gu = torch.empty((E, 2 * I), dtype=torch.float32, device=device)
+    q_d = torch.empty((E, H, I), dtype=torch.uint8, device=device)
+    s_d = torch.empty((E, H), dtype=torch.float32, device=device)
+    for e in range(E):
+        q_gu[e], s_gu[e] = fp8_rows(torch.randn(2 * I, H, generator=g, device=device) * std)
+    for e in range(E):
+        q_d[e], s_d[e] = fp8_rows(torch.randn(H, I, generator=g, device=device) * std)
+    return w_r, q_gu, s_gu, q_d, s_d
+
+
 def tokens(M: int, hidden: int, seed: int, device="cpu") -> torch.Tensor:
     """x [M, hidden] bf16 ~ N(0,1)."""
     return _randn_bf16((M, hidden), 1.0, _gen(seed, device), device)
