@@ -44,12 +44,13 @@ L2_BYTES = 126 * 1024 * 1024      # replaced by the device's value when a GPU is
 
 # --------------------------------------------------------------- helpers --
 
-def algorithmic_bytes(hidden, n_experts, topk, inter, M, n_active):
+def algorithmic_bytes(hidden, n_experts, topk, inter, M, n_active, fp8=False):
     """Bytes the layer must move per call: each distinct activated expert's
     gate/up and down weights once, the router weight once, x in, out out and
     the routing indices out.  Weights of experts nobody chose are not counted
-    (that is the work the routing avoids)."""
-    expert = 3 * hidden * inter * 2
+    (that is the work the routing avoids).  fp8: one byte per expert weight
+    plus the fp32 row scales ((2I + H) per expert); the router stays bf16."""
+    expert = 3 * hidden * inter + (2 * inter + hidden) * 4 if fp8 else 3 * hidden * inter * 2
     return (n_active * expert + n_experts * hidden * 2 + 2 * M * hidden * 2 + M * topk * 4)
 
 
@@ -63,7 +64,8 @@ def source_hash(paths):
 
 LAYER_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
                  for f in ("layer_kernel.cuh", "routing.cuh", "common.cuh", "kernels.cuh",
-                           "layer_kernel_a.cu", "layer_kernel_b.cu", "layer_kernel_c.cu", "layer_kernel_d.cu")]
+                           "layer_kernel_a.cu", "layer_kernel_b.cu", "layer_kernel_c.cu", "layer_kernel_d.cu",
+                           "layer_kernel_e.cu", "layer_kernel_f.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "layer_traffic.json")
 
 
@@ -168,13 +170,19 @@ def max_over_ranks(pg, v):
 class Workload:
     """Distinct layers on the device plus pools of token batches."""
 
-    def __init__(self, shape, n_layers, M, pool, zipf, device, layer_seed0=1000, variant=False):
+    def __init__(self, shape, n_layers, M, pool, zipf, device, layer_seed0=1000, variant=False, fp8=False):
         import torch
         from weight_streaming_expert_gb300 import MoELayer
         from weight_streaming_expert_gb300 import workloads as wl
         self.shape, self.M, self.device = shape, M, device
         self.layers = []
         for l in range(n_layers):
+            if fp8:  # E4M3 expert codes with fp32 row scales
+                w_r, q_gu, s_gu, q_d, s_d = wl.fp8_expert_weights(shape, seed=layer_seed0 + l, device=device)
+                self.layers.append(MoELayer.fp8(w_r, q_gu, s_gu, q_d, s_d, topk=shape.topk))
+                del w_r, q_gu, s_gu, q_d, s_d
+                torch.cuda.empty_cache()
+                continue
             w_r, w_gu, w_d = wl.layer_weights(shape, seed=layer_seed0 + l, device=device)
             kw = {}
             if variant:  # a shared expert, routed scale 2.5, the bias for selection only
@@ -217,13 +225,13 @@ class Workload:
         self.layers = []
 
 
-def n_layers_for(M, shape, l2_bytes, requested):
+def n_layers_for(M, shape, l2_bytes, requested, fp8=False):
     if requested:
         return requested
     # distinct layers so that >= 3 x L2 of other layers' weights stream
     # between two calls of the same layer (at least 4)
     est_active = min(M * shape.topk, shape.n_experts) * 0.85 + 1
-    per_call = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, est_active)
+    per_call = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, est_active, fp8)
     return max(4, int(math.ceil(3 * l2_bytes / per_call)) + 1)
 
 
@@ -425,12 +433,12 @@ def run_ours(args):
     l2 = getattr(prop, "L2_cache_size", L2_BYTES) or L2_BYTES
     shape = wl.SHAPES[args.shape]
     M = args.M
-    n_layers = n_layers_for(M, shape, l2, args.layers)
-    wkl = Workload(shape, n_layers, M, args.pool, args.zipf, dev, variant=args.variant)
+    n_layers = n_layers_for(M, shape, l2, args.layers, args.fp8)
+    wkl = Workload(shape, n_layers, M, args.pool, args.zipf, dev, variant=args.variant, fp8=args.fp8)
     ms, active, clocks = time_graph(wkl, args.steps, args.warmup, pg, sample_clocks=(rank == 0),
                                     gpu_index=local)
     mean_active = float(np.mean(active)) + (1.0 if args.variant else 0.0)  # + the shared expert
-    bytes_call = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, mean_active)
+    bytes_call = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, mean_active, args.fp8)
     us = ms * 1000.0
     gbs = bytes_call / (us * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
@@ -442,7 +450,7 @@ def run_ours(args):
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
         if (tr.get("source_hash") == source_hash(LAYER_SOURCES) and tr.get("M") == M
-                and args.shape == tr.get("shape", "ling") and not args.variant):
+                and args.shape == tr.get("shape", "ling") and not args.variant and not args.fp8):
             # measured on a smaller run (one layer, 8 calls): DRAM traffic
             # follows the algorithmic bytes, so scale it to this run's launches
             traffic = int(round(tr["bytes_per_launch"] * bytes_call / tr["algorithmic_bytes_per_launch"]))
@@ -457,7 +465,8 @@ def run_ours(args):
             wkl.new_pool(m2, args.pool)
             ms2, act2, _ = time_graph(wkl, min(args.steps, 4000), args.warmup, None)
             act2 = [a + (1 if args.variant else 0) for a in act2]
-            b2 = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, m2, float(np.mean(act2)))
+            b2 = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, m2, float(np.mean(act2)),
+                                   args.fp8)
             by_m[f"M={m2}" + ("_zipf" if z2 else "")] = {
                 "us_per_call": round(ms2 * 1000, 3), "achieved_gbs": round(b2 / (ms2 * 1e-3) / 1e9, 1),
                 "frac_of_peak": round(b2 / (ms2 * 1e-3) / 1e9 / peak, 4),
@@ -477,13 +486,14 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8 weights, bf16 tokens" if args.fp8 else "bf16",
             "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens (random init, no checkpoint)",
             "config": {"workload": f"Ling-shaped MoE {'block-verify' if M >= 16 else 'verify' if M > 1 else 'decode'} step"
                                    f"{' (per-GPU slice of a 4-way TP split)' if args.shape == 'ling_tp4' else ''}: "
                                    f"hidden {shape.hidden}, {shape.n_experts} experts, top-{shape.topk} softmax+renorm, "
                                    f"SwiGLU inter {shape.inter}, "
                                    f"{'+ shared expert, routed scale 2.5, bias for selection only, ' if args.variant else ''}"
+                                   f"{'fp8 E4M3 expert weights with fp32 row scales, ' if args.fp8 else ''}"
                                    f"M={M}, {'Zipf(1.1) router bias' if args.zipf else 'uniform routing'}",
                        "M": M, "layers_cycled": n_layers, "x_pool": args.pool,
                        "l2_policy": f"inputs larger than L2: {n_layers} distinct layer weight sets cycled, "
@@ -666,6 +676,7 @@ def main(argv=None):
                     help="skip the M=1 and M=16 (Zipf) side measurements")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle timing")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--fp8", action="store_true", help="layers with fp8 (E4M3) expert weights and row scales")
     ap.add_argument("--variant", action="store_true",
                     help="layers with a shared expert, routed scale 2.5 and the router bias for selection only")
     ap.add_argument("--lm-head", dest="lm_head", action="store_true",

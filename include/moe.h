@@ -144,6 +144,29 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter,
                            const void* w_down, const moe_layer_opts_t* opts);
 
 /*
+ * moe_create_fp8 -- a layer whose expert weights are fp8 (the post: "once
+ * fp8 weights shrink the fixed base"): OCP E4M3 codes with one fp32 scale
+ * per output row, so the dequantized matrix is diag(scale) * decode(codes);
+ * each expert GEMV sums x * code in fp32 and applies the row scale after
+ * the sum.  The router stays bf16.  The forward call and its outputs are
+ * those of moe_create's layers; the activations and h are taken to f16 on
+ * the chip (exact for |values| within f16's normal range, 6.1e-5 .. 65504).
+ *   w_router   device bf16 [E][H] (16-byte aligned).
+ *   q_gate_up  device uint8 [E][2I][H] E4M3 codes (gate rows first), 16-byte
+ *              aligned;      s_gate_up device fp32 [E][2I], 4-byte aligned.
+ *   q_down     device uint8 [E][H][I] E4M3 codes, 16-byte aligned;
+ *              s_down     device fp32 [E][H], 4-byte aligned.
+ * hidden, n_experts, topk, inter as moe_create.  The codes and scales are
+ * copied (codes re-laid out into 16-row tiles); the caller may free them.
+ * Streams half the bytes of a bf16 layer per activated expert (3*H*I bytes
+ * + (2I + H) * 4 bytes of scales).  Errors as moe_create.
+ */
+moe_layer_t* moe_create_fp8(int hidden, int n_experts, int topk, int inter,
+                            const void* w_router, const void* q_gate_up,
+                            const float* s_gate_up, const void* q_down,
+                            const float* s_down);
+
+/*
  * moe_forward -- run the layer on M tokens, asynchronously on `stream`.
  *   x         device bf16 [M][H], 16-byte aligned, read only.
  *   out       device bf16 [M][H]: out[m] = bf16( sum_j w[m][j] * y_j ),
@@ -213,9 +236,11 @@ typedef struct {
   int n_sms;               /* SMs of the device the handle lives on */
   int gateup_stages;       /* shared-memory ring depth of the gate/up phase */
   int down_stages;         /* shared-memory stages of the down phase */
-  int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 rows x H) */
+  int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 bf16 or
+                              16 fp8 rows x H) */
   int down_tile_bytes;     /* bytes of one down super tile (8 slabs of
-                              8 rows x I, one per consumer warp) */
+                              8 bf16 or 16 fp8 rows x I, one per consumer
+                              warp) */
   size_t weight_bytes;     /* device bytes held for the weights */
   size_t workspace_bytes;  /* device bytes held for the workspace */
   int kernels_per_forward; /* kernel launches per forward call (1) */
@@ -224,6 +249,7 @@ typedef struct {
   int shared_expert;       /* 1 if the layer has a shared expert */
   float routed_scale;      /* factor on every routed weight */
   int bias_selection_only; /* 1 if the router bias only picks the experts */
+  int fp8_experts;         /* 1 if the expert weights are E4M3 codes */
 } moe_info_t;
 
 int moe_get_info(const moe_layer_t* h, moe_info_t* out);

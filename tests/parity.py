@@ -63,12 +63,11 @@ def compare_outputs(gpu_out_f32, ora_out_bits):
     return max_abs, rel
 
 
-def check_layer(orc, x_bits, wr_bits, wgu_bits, wd_bits, k, gpu_out_f32, gpu_idx, bias=None,
-                max_abs=MAX_ABS, max_rel=MAX_REL_L2, **variant):
-    """Full acceptance check; returns a dict of stats, raises AssertionError on failure.
-    ``variant``: the oracle's layer-variant arguments (shared_gate_up,
-    shared_down, routed_scale, bias_selection_only)."""
-    ref = orc.moe_forward(x_bits, wr_bits, wgu_bits, wd_bits, k, bias=bias, **variant)
+def check_against(ref_fn, gpu_out_f32, gpu_idx, max_abs=MAX_ABS, max_rel=MAX_REL_L2):
+    """The acceptance rule against any oracle layer: ref_fn(idx_in) returns the
+    oracle's dict (out, idx, logits, ...) with its own routing (idx_in None) or
+    scored on the GPU's experts.  Returns stats; raises AssertionError."""
+    ref = ref_fn(None)
     gpu_idx = np.asarray(gpu_idx, np.int32)
     ties = 0
     for m in range(gpu_idx.shape[0]):
@@ -78,8 +77,18 @@ def check_layer(orc, x_bits, wr_bits, wgu_bits, wd_bits, k, gpu_out_f32, gpu_idx
                 f"is not a near-tie")
             ties += 1
     if ties:
-        ref = orc.moe_forward(x_bits, wr_bits, wgu_bits, wd_bits, k, bias=bias, idx_in=gpu_idx, **variant)
+        ref = ref_fn(gpu_idx)
     max_abs_err, rel = compare_outputs(gpu_out_f32, ref["out"])
     assert max_abs_err <= max_abs and rel <= max_rel, (
         f"outputs: max-abs {max_abs_err:.3e} (<= {max_abs}) rel-L2 {rel:.3e} (<= {max_rel})")
     return dict(near_tie_tokens=ties, max_abs=max_abs_err, rel_l2=rel, ref=ref)
+
+
+def check_layer(orc, x_bits, wr_bits, wgu_bits, wd_bits, k, gpu_out_f32, gpu_idx, bias=None,
+                max_abs=MAX_ABS, max_rel=MAX_REL_L2, **variant):
+    """Full acceptance check; returns a dict of stats, raises AssertionError on failure.
+    ``variant``: the oracle's layer-variant arguments (shared_gate_up,
+    shared_down, routed_scale, bias_selection_only)."""
+    return check_against(lambda ii: orc.moe_forward(x_bits, wr_bits, wgu_bits, wd_bits, k, bias=bias, idx_in=ii,
+                                                    **variant),
+                         gpu_out_f32, gpu_idx, max_abs, max_rel)

@@ -482,3 +482,54 @@ def test_variant_routing_outputs(oracle, ling_variant):
     assert shared_groups.sum() == 1 and r["grp_cnt"][shared_groups][0] == M
     assert sorted(r["pair_list"].tolist()) == list(range(M * (k + 1)))
     layer.set_router_bias(None)
+
+
+# ------------------------------------------------------ fp8 expert weights --
+# E4M3 codes with fp32 per-row scales (the oracle's moe_forward_fp8).
+
+def fp8_layer(MoELayer, shape, seed, device="cpu"):
+    w_r, q_gu, s_gu, q_d, s_d = wl.fp8_expert_weights(shape, seed=seed, device=device)
+    layer = MoELayer.fp8(w_r.to(DEV), q_gu.to(DEV), s_gu.to(DEV), q_d.to(DEV), s_d.to(DEV), topk=shape.topk)
+    host = dict(wr=bits(w_r), q_gu=q_gu.cpu().numpy(), s_gu=s_gu.cpu().numpy(), q_d=q_d.cpu().numpy(),
+                s_d=s_d.cpu().numpy())
+    return layer, host
+
+
+def run_and_check_fp8(orc, layer, host, x, k, bias=None):
+    layer.set_router_bias(bias)
+    out, idx = layer(x)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    xb = bits(x)
+    b = None if bias is None else bias.cpu().numpy()
+    return parity.check_against(
+        lambda ii: orc.moe_forward_fp8(xb, host["wr"], host["q_gu"], host["s_gu"], host["q_d"], host["s_d"], k,
+                                       bias=b, idx_in=ii),
+        out.float().cpu().numpy(), idx.cpu().numpy())
+
+
+@pytest.mark.parametrize("H,E,k,I,M", [(256, 16, 2, 128, 1), (256, 16, 2, 128, 7), (512, 64, 6, 256, 16),
+                                       (1280, 40, 3, 256, 23), (2560, 24, 2, 512, 64), (1024, 96, 8, 512, 9)])
+def test_fp8_small(oracle, MoELayer, H, E, k, I, M):
+    shape = wl.LayerShape(hidden=H, n_experts=E, topk=k, inter=I)
+    layer, host = fp8_layer(MoELayer, shape, seed=H + E + k + 99)
+    assert layer.info().fp8_experts == 1
+    x = wl.tokens(M, H, seed=M + 900).to(DEV)
+    run_and_check_fp8(oracle, layer, host, x, k)
+    layer.close()
+
+
+@pytest.fixture(scope="module")
+def ling_fp8(MoELayer):
+    layer, host = fp8_layer(MoELayer, wl.LING, seed=1300, device=DEV)
+    torch.cuda.empty_cache()
+    yield layer, host
+    layer.close()
+
+
+@pytest.mark.parametrize("M,zipf", [(6, False), (1, False), (16, True), (64, False)])
+def test_ling_fp8(oracle, ling_fp8, M, zipf):
+    layer, host = ling_fp8
+    bias = wl.zipf_router_bias(wl.LING.n_experts) if zipf else None
+    x = wl.tokens(M, wl.LING.hidden, seed=7_000_000 + M, device=DEV)
+    run_and_check_fp8(oracle, layer, host, x, wl.LING.topk, bias=bias)

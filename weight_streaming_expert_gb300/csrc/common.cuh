@@ -194,6 +194,36 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // bf16x2 (low element first in memory) -> two fp32, exact.
+// D = A(16x16, row) * B(16x8, col) + D, f16 inputs, fp32 accumulate (the
+// fp8-weight path: codes and activations are exact in f16).
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four E4M3 codes (bytes 0..3 of v) -> two f16x2 in the same element order
+// (bytes 0, 1 -> lo; 2, 3 -> hi).  Exact: every E4M3 value is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 p, q; mov.b32 {p, q}, %2; cvt.rn.f16x2.e4m3x2 %0, p; cvt.rn.f16x2.e4m3x2 %1, q; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+
+// bf16x2 -> f16x2, element order kept; exact for values in f16's normal
+// range (bf16's 8-bit significand fits f16's 11).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(v & 0xffff0000u)), "f"(__uint_as_float(v << 16)));
+  return d;
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 

@@ -15,6 +15,8 @@ struct LayerArgs {
   const float* bias;              // [E] or nullptr
   const uint8_t* w_gate_up;       // packed gate/up tiles, see pack.cu
   const uint8_t* w_down;          // packed down tiles, see pack.cu
+  const float* s_gu;              // fp8 experts: [E][2I] gate/up row scales (else unused)
+  const float* s_d;               // fp8 experts: [E][H] down row scales (else unused)
   __nv_bfloat16* out;             // [M][H]
   int32_t* topk_idx;              // [M][K] caller output
   float* topk_w;                  // [M][K] caller output or nullptr
@@ -35,17 +37,21 @@ struct LayerArgs {
 // The layer kernel: grid = #SMs x kExpertThreads, dynamic shared memory
 // layer_smem_bytes(ring_bytes, NP, buckets).  KPW = H/256.
 using LayerKernel = void (*)(LayerArgs);
-// variant: the instance that handles the layer variants (nullptr: no such
-// kpw).
-LayerKernel layer_kernel_for(int kpw, bool variant);
+// variant: the instance that handles the layer variants; fp8: the instance
+// for E4M3 expert weights (plain layers only).  nullptr: no such instance.
+LayerKernel layer_kernel_for(int kpw, bool variant, bool fp8 = false);
 size_t layer_smem_bytes(uint32_t ring_bytes, int NP, int E);
-// Bytes of the reduction area that follows the gate/up stages.
-uint32_t layer_reduction_bytes();
+// Bytes of the reduction area that follows the gate/up stages (fp8 tiles
+// hold two n8 blocks: twice the partials).
+uint32_t layer_reduction_bytes(bool fp8 = false);
 
 // Create-time re-layout (pack.cu).
 void pack_gate_up(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int I, int H,
                   cudaStream_t s);
 void pack_down(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int H, int I, cudaStream_t s);
+// E4M3 codes: gate/up tiles of 16 rows, down slabs of 16 rows (pack.cu).
+void pack_gate_up_fp8(const uint8_t* src, uint8_t* dst, int E, int I, int H, cudaStream_t s);
+void pack_down_fp8(const uint8_t* src, uint8_t* dst, int E, int H, int I, cudaStream_t s);
 
 // Set the calling thread's moe_last_error() text (moe_api.cu).
 void set_last_error_text(const char* text);

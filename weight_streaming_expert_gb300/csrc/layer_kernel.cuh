@@ -169,13 +169,20 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g));
 // KPW = H / 256: 32-wide k chunks per warp in the gate/up GEMV.  VARIANT:
 // the instance that handles the layer variants (shared expert, routed scale,
 // selection-only bias); the plain instance compiles none of their code.
-template <int KPW, bool VARIANT>
+// FP8: expert weights as E4M3 codes with fp32 per-row scales -- tiles of 16
+// rows (the same bytes as 8 bf16 rows), codes converted to f16 in registers,
+// tokens and h converted to f16 per group, the row scales applied in fp32
+// after the sums (reducer and down epilogue).
+template <int KPW, bool VARIANT, bool FP8>
 __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs a) {
   using namespace layer_detail;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) stamp(a, 19);  // CTA started
   const int S = a.gu_stages;
+  constexpr int GU_ROWS = FP8 ? 16 : kGateUpTileRows;  // weight rows per gate/up tile
+  constexpr int D_ROWS = FP8 ? 16 : kDownTileRows;     // output rows per down slab
+  constexpr int NB = FP8 ? 2 : 1;                      // n8 blocks per tile (partials per lane)
   const int NSL = kConsumerWarps, SD = a.d_stages;  // slabs per down super tile, down slots
   const int MK = a.M * a.K;                     // routed pairs (token * K + slot)
   const bool shared = VARIANT && a.shared;
@@ -311,9 +318,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   }
   if (tid == 0) stamp(a, 3);
 
-  const int TPG = 2 * a.I / kGateUpTileRows;  // gate/up tiles per group
+  const int TPG = 2 * a.I / GU_ROWS;          // gate/up tiles per group
   const int T_gu = n_groups * TPG;
-  const int SL = a.H / kDownTileRows;         // 8-row output slabs per group
+  const int SL = a.H / D_ROWS;                // output slabs per group (the down GEMV's unit)
   const int SPG = SL / NSL;                   // down super tiles per group
   const int T_d = n_groups * SPG;
   // groups [0, g_static) are split statically in both GEMVs: their gate/up
@@ -578,28 +585,62 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         for (int q = 0; q < KPW; ++q) {
           xa[q] = x0[4 * (warp * KPW + q)];
           xb[q] = x1[4 * (warp * KPW + q)];
+          if constexpr (FP8) {
+            xa[q] = bf16x8_to_f16x8(xa[q]);
+            xb[q] = bf16x8_to_f16x8(xb[q]);
+          }
         }
         cur_g = g;
+      }
+      float2 sc[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};  // (gate, up) row scales per block
+      if constexpr (FP8) {
+        if (warp == (j & (kRedSlots - 1))) {  // this tile's reducer: its rows' scales, early
+          const float* sg = a.s_gu + (size_t)rt.grp_expert[g] * 2 * a.I;
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int r = 8 * tt + 4 * b + t4;
+            sc[b] = make_float2(__ldg(sg + r), __ldg(sg + a.I + r));
+          }
+        }
       }
       if (!warp_wait(full(s), ph, &waited)) {
         record_timeout(a.ws, 2, kErrTimeoutFull, j, S, full(s), waited);
         break;
       }
       if (j == 0 && tid == 0) stamp(a, 4);
+      // bf16: c0, c1 = the two k-steps of the one n8 block; fp8: c0, c1 = the
+      // two n8 blocks, each over both k-steps
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const uint4* wp = reinterpret_cast<const uint4*>(ring + (size_t)s * a.gu_tile) + (warp * KPW) * 32 + lane;
 #pragma unroll
       for (int q = 0; q < KPW; ++q) {
         const uint4 b = wp[q * 32];
-        mma_bf16(c0, xa[q].x, xb[q].x, xa[q].y, xb[q].y, b.x, b.y);
-        mma_bf16(c1, xa[q].z, xb[q].z, xa[q].w, xb[q].w, b.z, b.w);
+        if constexpr (FP8) {  // b.x, b.y: block 0 row g4 (8 codes); b.z, b.w: block 1 row g4
+          uint32_t f0, f1, f2, f3;
+          e4m3x4_to_f16x2(b.x, f0, f1);
+          e4m3x4_to_f16x2(b.y, f2, f3);
+          mma_f16(c0, xa[q].x, xb[q].x, xa[q].y, xb[q].y, f0, f1);
+          mma_f16(c0, xa[q].z, xb[q].z, xa[q].w, xb[q].w, f2, f3);
+          e4m3x4_to_f16x2(b.z, f0, f1);
+          e4m3x4_to_f16x2(b.w, f2, f3);
+          mma_f16(c1, xa[q].x, xb[q].x, xa[q].y, xb[q].y, f0, f1);
+          mma_f16(c1, xa[q].z, xb[q].z, xa[q].w, xb[q].w, f2, f3);
+        } else {
+          mma_bf16(c0, xa[q].x, xb[q].x, xa[q].y, xb[q].y, b.x, b.y);
+          mma_bf16(c1, xa[q].z, xb[q].z, xa[q].w, xb[q].w, b.z, b.w);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty(s));  // stage free for the producer
 
       const int slot = j & (kRedSlots - 1);
-      red[(slot * kConsumerWarps + warp) * 32 + lane] =
-          make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
+      if constexpr (FP8) {
+        red[((slot * kConsumerWarps + warp) * 32 + lane) * NB] = make_float4(c0[0], c0[1], c0[2], c0[3]);
+        red[((slot * kConsumerWarps + warp) * 32 + lane) * NB + 1] = make_float4(c1[0], c1[1], c1[2], c1[3]);
+      } else {
+        red[(slot * kConsumerWarps + warp) * 32 + lane] =
+            make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(redbar(slot));
       if (warp == slot) {  // this tile's reducer (rotates over the warps)
@@ -607,21 +648,30 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
           record_timeout(a.ws, 2, kErrTimeoutReduce, j, S, redbar(slot), waited);
           break;
         }
-        float4 acc = red[(slot * kConsumerWarps) * 32 + lane];
 #pragma unroll
-        for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
-          const float4 v = red[(slot * kConsumerWarps + w2) * 32 + lane];
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
+        for (int b = 0; b < NB; ++b) {
+          float4 acc = red[((slot * kConsumerWarps) * 32 + lane) * NB + b];
+#pragma unroll
+          for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
+            const float4 v = red[((slot * kConsumerWarps + w2) * 32 + lane) * NB + b];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
+          // (acc.x, acc.y) = (gate, up) of group token g4, intermediate row
+          // GU_ROWS/2 tt + 4 b + t4; (acc.z, acc.w) the same for token g4 + 8
+          const int r = (GU_ROWS / 2) * tt + 4 * b + t4;
+          if constexpr (FP8) {  // the row scales, after the sums
+            acc.x *= sc[b].x;
+            acc.z *= sc[b].x;
+            acc.y *= sc[b].y;
+            acc.w *= sc[b].y;
+          }
+          if (g4 < cnt) a.ws.h[(size_t)(start + g4) * a.I + r] = __float2bfloat16_rn(silu(acc.x) * acc.y);
+          if (g4 + 8 < cnt)
+            a.ws.h[(size_t)(start + g4 + 8) * a.I + r] = __float2bfloat16_rn(silu(acc.z) * acc.w);
         }
-        // (acc.x, acc.y) = (gate, up) of group token g4, intermediate row
-        // 4 tt + t4; (acc.z, acc.w) the same for group token g4 + 8
-        const int r = 4 * tt + t4;
-        if (g4 < cnt) a.ws.h[(size_t)(start + g4) * a.I + r] = __float2bfloat16_rn(silu(acc.x) * acc.y);
-        if (g4 + 8 < cnt)
-          a.ws.h[(size_t)(start + g4 + 8) * a.I + r] = __float2bfloat16_rn(silu(acc.z) * acc.w);
       }
       if (j == n_static - 1) {  // every static tile of this warp's share is reduced
         __syncwarp();
@@ -644,7 +694,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     uint4 ha[kMaxDownChunks], hb[kMaxDownChunks];
     int pid0 = -1, pid1 = -1;
     float pw0 = 0.f, pw1 = 0.f;
-    int cur_g = -1;
+    int cur_g = -1, cur_de = 0;
     for (int j = 0;; ++j) {
       const int s = j % SD;
       const uint32_t ph = (uint32_t)(j / SD) & 1u;
@@ -667,19 +717,32 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
           if (q < kpd) {
             ha[q] = __ldcg(h0 + 4 * q);  // written by other SMs in this grid: L2, not L1
             hb[q] = __ldcg(h1 + 4 * q);
+            if constexpr (FP8) {
+              ha[q] = bf16x8_to_f16x8(ha[q]);
+              hb[q] = bf16x8_to_f16x8(hb[q]);
+            }
           }
         }
+        if constexpr (FP8) cur_de = rt.grp_expert[g];
         pid0 = g4 < cnt ? rt.pair_list[start + g4] : -1;
         pid1 = g4 + 8 < cnt ? rt.pair_list[start + g4 + 8] : -1;
         pw0 = pid0 >= 0 ? rt.s_w[pid0] : 0.f;
         pw1 = pid1 >= 0 ? rt.s_w[pid1] : 0.f;
         cur_g = g;
       }
+      float2 rs[NB];  // fp8: the output rows' scales, loaded while the data lands
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        rs[b] = make_float2(1.f, 1.f);
+        if constexpr (FP8)
+          rs[b] = __ldg(reinterpret_cast<const float2*>(a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + 8 * b + 2 * t4));
+      }
       if (!warp_wait(dfull(s), ph, &waited)) {
         record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dfull(s), waited);
         break;
       }
       if (j == 0 && tid == 0) stamp(a, 14);
+      // bf16: c0, c1 = the two k-steps; fp8: c0, c1 = the two n8 blocks
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const uint4* bp =
           reinterpret_cast<const uint4*>(ring + (size_t)cell_tab[s * kConsumerWarps + warp] * a.d_tile) + lane;
@@ -687,20 +750,38 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       for (int q = 0; q < kMaxDownChunks; ++q) {
         if (q < kpd) {
           const uint4 b = bp[q * 32];
-          mma_bf16(c0, ha[q].x, hb[q].x, ha[q].y, hb[q].y, b.x, b.y);
-          mma_bf16(c1, ha[q].z, hb[q].z, ha[q].w, hb[q].w, b.z, b.w);
+          if constexpr (FP8) {  // b.x, b.y: output row g4 of block 0; b.z, b.w: of block 1
+            uint32_t f0, f1, f2, f3;
+            e4m3x4_to_f16x2(b.x, f0, f1);
+            e4m3x4_to_f16x2(b.y, f2, f3);
+            mma_f16(c0, ha[q].x, hb[q].x, ha[q].y, hb[q].y, f0, f1);
+            mma_f16(c0, ha[q].z, hb[q].z, ha[q].w, hb[q].w, f2, f3);
+            e4m3x4_to_f16x2(b.z, f0, f1);
+            e4m3x4_to_f16x2(b.w, f2, f3);
+            mma_f16(c1, ha[q].x, hb[q].x, ha[q].y, hb[q].y, f0, f1);
+            mma_f16(c1, ha[q].z, hb[q].z, ha[q].w, hb[q].w, f2, f3);
+          } else {
+            mma_bf16(c0, ha[q].x, hb[q].x, ha[q].y, hb[q].y, b.x, b.y);
+            mma_bf16(c1, ha[q].z, hb[q].z, ha[q].w, hb[q].w, b.z, b.w);
+          }
         }
       }
       __syncwarp();  // every lane has read the stage
       if (lane == 0) mbar_arrive(dempty(s));
-      // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of the slab)
-      const int row = sl * kDownTileRows + 2 * t4;
-      if (pid0 >= 0)
-        *reinterpret_cast<float2*>(a.ws.y + (size_t)pid0 * a.H + row) =
-            make_float2(pw0 * (c0[0] + c1[0]), pw0 * (c0[1] + c1[1]));
-      if (pid1 >= 0)
-        *reinterpret_cast<float2*>(a.ws.y + (size_t)pid1 * a.H + row) =
-            make_float2(pw1 * (c0[2] + c1[2]), pw1 * (c0[3] + c1[3]));
+      // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of block b of the slab)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const int row = sl * D_ROWS + 8 * b + 2 * t4;
+        float v[4];  // (token g4 | g4 + 8) x (rows row, row + 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = FP8 ? (b ? c1[i] : c0[i]) : c0[i] + c1[i];
+        if (pid0 >= 0)
+          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid0 * a.H + row) =
+              make_float2(pw0 * (rs[b].x * v[0]), pw0 * (rs[b].y * v[1]));
+        if (pid1 >= 0)
+          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid1 * a.H + row) =
+              make_float2(pw1 * (rs[b].x * v[2]), pw1 * (rs[b].y * v[3]));
+      }
     }
     if (tid == 0) stamp(a, 7);
   }
@@ -710,8 +791,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   // each token's k rows summed in slot order, ONE bf16 rounding.  The other
   // CTAs count themselves in and leave at once, so the next call's CTAs get
   // their SMs (and run their prologue) while the combine runs.
-  const int n_own_ctas = min((int)gridDim.x, (SL + kConsumerWarps - 1) / kConsumerWarps);
-  const int own_per = (SL + n_own_ctas - 1) / n_own_ctas;  // 8 unless the grid is small
+  const int SLc = a.H / kDownTileRows;  // 8-row output slabs of the combine
+  const int n_own_ctas = min((int)gridDim.x, (SLc + kConsumerWarps - 1) / kConsumerWarps);
+  const int own_per = (SLc + n_own_ctas - 1) / n_own_ctas;  // 8 unless the grid is small
   const bool owner = (int)blockIdx.x < n_own_ctas;
   consumers_sync();
   if (tid == 0) {
@@ -723,7 +805,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   if (tid == 0) stamp(a, 15);
   const int nthr = kConsumerWarps * 32;
   const int sl0 = (int)blockIdx.x * own_per;
-  const int n_own = max(0, min(own_per, SL - sl0));
+  const int n_own = max(0, min(own_per, SLc - sl0));
   const int per = a.M * kDownTileRows;
   for (int it = tid; it < n_own * per; it += nthr) {
     const int sl = sl0 + it / per;

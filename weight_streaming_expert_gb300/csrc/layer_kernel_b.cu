@@ -1,15 +1,15 @@
 // layer_kernel_b.cu -- layer kernel instances for hidden = 256 x {8,10,12,16}, plain
-// (four translation units so that the instances compile in parallel).
+// (one of six translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {
 
 LayerKernel layer_kernel_plain_large(int kpw) {
   switch (kpw) {
-    case 8: return moe_layer_kernel<8, false>;
-    case 10: return moe_layer_kernel<10, false>;
-    case 12: return moe_layer_kernel<12, false>;
-    case 16: return moe_layer_kernel<16, false>;
+    case 8: return moe_layer_kernel<8, false, false>;
+    case 10: return moe_layer_kernel<10, false, false>;
+    case 12: return moe_layer_kernel<12, false, false>;
+    case 16: return moe_layer_kernel<16, false, false>;
     default: return nullptr;
   }
 }
@@ -17,8 +17,15 @@ LayerKernel layer_kernel_plain_large(int kpw) {
 LayerKernel layer_kernel_plain_small(int kpw);
 LayerKernel layer_kernel_variant_small(int kpw);
 LayerKernel layer_kernel_variant_large(int kpw);
+LayerKernel layer_kernel_fp8_small(int kpw);
+LayerKernel layer_kernel_fp8_large(int kpw);
 
-LayerKernel layer_kernel_for(int kpw, bool variant) {
+LayerKernel layer_kernel_for(int kpw, bool variant, bool fp8) {
+  if (fp8) {
+    if (variant) return nullptr;  // fp8 experts: plain layers only
+    const LayerKernel k = layer_kernel_fp8_large(kpw);
+    return k ? k : layer_kernel_fp8_small(kpw);
+  }
   if (variant) {
     const LayerKernel k = layer_kernel_variant_large(kpw);
     return k ? k : layer_kernel_variant_small(kpw);

@@ -1,15 +1,15 @@
 // layer_kernel_d.cu -- layer kernel instances for hidden = 256 x {8,10,12,16}, layer variants
-// (four translation units so that the instances compile in parallel).
+// (one of six translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {
 
 LayerKernel layer_kernel_variant_large(int kpw) {
   switch (kpw) {
-    case 8: return moe_layer_kernel<8, true>;
-    case 10: return moe_layer_kernel<10, true>;
-    case 12: return moe_layer_kernel<12, true>;
-    case 16: return moe_layer_kernel<16, true>;
+    case 8: return moe_layer_kernel<8, true, false>;
+    case 10: return moe_layer_kernel<10, true, false>;
+    case 12: return moe_layer_kernel<12, true, false>;
+    case 16: return moe_layer_kernel<16, true, false>;
     default: return nullptr;
   }
 }

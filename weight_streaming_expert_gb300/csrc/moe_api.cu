@@ -70,6 +70,9 @@ struct moe_layer {
   int shared = 0;           // 1: expert E (packed after the routed ones) is a shared expert
   float routed_scale = 1.0f;
   int sel_only = 0;         // the router bias picks the experts only
+  int fp8 = 0;              // expert weights are E4M3 codes with per-row scales
+  float* sc_gu = nullptr;   // fp8: [E][2I] gate/up row scales
+  float* sc_d = nullptr;    // fp8: [E][H] down row scales
   int kp() const { return K + shared; }  // pairs per token
   int ea() const { return E + shared; }  // packed experts
   int dev = 0, n_sms = 0;
@@ -100,6 +103,8 @@ void free_layer(moe_layer* h) {
   cudaFree(h->w_router);
   cudaFree(h->w_gu);
   cudaFree(h->w_d);
+  cudaFree(h->sc_gu);
+  cudaFree(h->sc_d);
   cudaFree(h->bias);
   cudaFree(h->ws_mem);
   delete h;
@@ -126,6 +131,8 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   la.bias = h->bias;
   la.w_gate_up = h->w_gu;
   la.w_down = h->w_d;
+  la.s_gu = h->sc_gu;
+  la.s_d = h->sc_d;
   la.out = static_cast<__nv_bfloat16*>(out);
   la.topk_idx = idx;
   la.topk_w = tw;
@@ -188,13 +195,15 @@ extern "C" {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const void* w_router,
-                        const void* w_gate_up, const void* w_down) {
-  return moe_create_ex(hidden, n_experts, topk, inter, w_router, w_gate_up, w_down, nullptr);
-}
+}  // extern "C"
 
-moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const void* w_router,
-                           const void* w_gate_up, const void* w_down, const moe_layer_opts_t* opts) {
+namespace {
+
+// The create path of moe_create, moe_create_ex and moe_create_fp8: fp8 ->
+// w_gate_up / w_down are E4M3 codes with row scales s_gu / s_d (no variants).
+moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const void* w_router,
+                        const void* w_gate_up, const void* w_down, const moe_layer_opts_t* opts, const float* s_gu,
+                        const float* s_d, bool fp8) {
   g_last_error.clear();
   // ---- argument checks (no CUDA call before these pass) ----
   if (hidden <= 0 || hidden % 256 != 0 || !layer_kernel_for(hidden / 256, false)) {
@@ -231,6 +240,10 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
     return nullptr;
   }
   const int shared = o.w_shared_gate_up ? 1 : 0;
+  if (fp8 && (!s_gu || !s_d || (reinterpret_cast<uintptr_t>(s_gu) & 3u) || (reinterpret_cast<uintptr_t>(s_d) & 3u))) {
+    set_err("fp8 experts: the row scales must be non-null, 4-byte aligned device pointers");
+    return nullptr;
+  }
 
   // ---- device ----
   int dev = 0;
@@ -244,7 +257,7 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
   }
   cudaFuncAttributes fa;
   const bool variant = o.w_shared_gate_up || o.bias_selection_only || (o.routed_scale > 0.f && o.routed_scale != 1.0f);
-  if ((e = cudaFuncGetAttributes(&fa, layer_kernel_for(hidden / 256, variant))) != cudaSuccess) {
+  if ((e = cudaFuncGetAttributes(&fa, layer_kernel_for(hidden / 256, variant, fp8))) != cudaSuccess) {
     cuda_fail(e, "kernel image");
     return nullptr;
   }
@@ -254,9 +267,10 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
   h->shared = shared;
   h->routed_scale = o.routed_scale > 0.f ? o.routed_scale : 1.0f;
   h->sel_only = o.bias_selection_only ? 1 : 0;
+  h->fp8 = fp8 ? 1 : 0;
   h->dev = dev;
   h->n_sms = prop.multiProcessorCount;
-  h->kernel = layer_kernel_for(hidden / 256, variant);
+  h->kernel = layer_kernel_for(hidden / 256, variant, fp8);
   h->tile_gu = (uint32_t)(kGateUpTileRows * hidden * 2);
   h->tile_d = (uint32_t)(kDownTileRows * inter * 2);
   h->ks = gemv_split(hidden, n_experts, h->n_sms);
@@ -270,7 +284,7 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
   const int np_max = kMaxTokens * h->kp();
   const size_t fixed = layer_smem_bytes(0, np_max, h->ea());
   const size_t avail = optin > fixed ? optin - fixed : 0;
-  const size_t red = layer_reduction_bytes();
+  const size_t red = layer_reduction_bytes(fp8);
   h->s_gu = avail > red ? (int)std::min<size_t>(kMaxGateUpStages, (avail - red) / h->tile_gu) : 0;
   // The down phase reuses the ring as slab-sized cells (a gate/up tile is
   // hidden/inter whole slabs of 8 rows x I); a down slot is 8 cells, one
@@ -287,11 +301,15 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
   AllocCounter ac;
   const size_t E = n_experts, H = hidden, I = inter;
   const size_t EA = (size_t)h->ea();  // routed experts, then the shared one
-  const size_t b_router = E * H * 2, b_gu = EA * 2 * I * H * 2, b_d = EA * H * I * 2;
-  h->weight_bytes = b_router + b_gu + b_d;
+  const size_t wb = fp8 ? 1 : 2;  // bytes per expert weight element
+  const size_t b_router = E * H * 2, b_gu = EA * 2 * I * H * wb, b_d = EA * H * I * wb;
+  const size_t b_sgu = fp8 ? E * 2 * I * 4 : 0, b_sd = fp8 ? E * H * 4 : 0;
+  h->weight_bytes = b_router + b_gu + b_d + b_sgu + b_sd;
   if (ac.alloc((void**)&h->w_router, b_router) != cudaSuccess ||
       ac.alloc((void**)&h->w_gu, b_gu) != cudaSuccess ||
-      ac.alloc((void**)&h->w_d, b_d) != cudaSuccess) {
+      ac.alloc((void**)&h->w_d, b_d) != cudaSuccess ||
+      (fp8 && (ac.alloc((void**)&h->sc_gu, b_sgu) != cudaSuccess ||
+               ac.alloc((void**)&h->sc_d, b_sd) != cudaSuccess))) {
     cudaGetLastError();
     set_err("device allocation of %zu weight bytes failed", h->weight_bytes);
     free_layer(h);
@@ -342,7 +360,13 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
   h->cap_stream = s;
   bool ok = cudaMemsetAsync(h->ws_mem, 0, h->ws_bytes, s) == cudaSuccess &&
             cudaMemcpyAsync(h->w_router, w_router, b_router, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
-  if (ok) {
+  if (ok && fp8) {
+    pack_gate_up_fp8(static_cast<const uint8_t*>(w_gate_up), h->w_gu, n_experts, inter, hidden, s);
+    pack_down_fp8(static_cast<const uint8_t*>(w_down), h->w_d, n_experts, hidden, inter, s);
+    ok = cudaMemcpyAsync(h->sc_gu, s_gu, b_sgu, cudaMemcpyDeviceToDevice, s) == cudaSuccess &&
+         cudaMemcpyAsync(h->sc_d, s_d, b_sd, cudaMemcpyDeviceToDevice, s) == cudaSuccess &&
+         cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
+  } else if (ok) {
     pack_gate_up(static_cast<const __nv_bfloat16*>(w_gate_up), reinterpret_cast<__nv_bfloat16*>(h->w_gu),
                  n_experts, inter, hidden, s);
     pack_down(static_cast<const __nv_bfloat16*>(w_down), reinterpret_cast<__nv_bfloat16*>(h->w_d),
@@ -371,6 +395,27 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const
   }
   return h;
 }
+
+}  // namespace
+
+extern "C" {
+
+moe_layer_t* moe_create(int hidden, int n_experts, int topk, int inter, const void* w_router,
+                        const void* w_gate_up, const void* w_down) {
+  return create_layer(hidden, n_experts, topk, inter, w_router, w_gate_up, w_down, nullptr, nullptr, nullptr, false);
+}
+
+moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter, const void* w_router,
+                           const void* w_gate_up, const void* w_down, const moe_layer_opts_t* opts) {
+  return create_layer(hidden, n_experts, topk, inter, w_router, w_gate_up, w_down, opts, nullptr, nullptr, false);
+}
+
+moe_layer_t* moe_create_fp8(int hidden, int n_experts, int topk, int inter, const void* w_router,
+                            const void* q_gate_up, const float* s_gate_up, const void* q_down,
+                            const float* s_down) {
+  return create_layer(hidden, n_experts, topk, inter, w_router, q_gate_up, q_down, nullptr, s_gate_up, s_down, true);
+}
+
 
 int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, float* topk_w, int M,
                    moe_stream_t stream, unsigned flags) {
@@ -501,6 +546,7 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
   o->shared_expert = h->shared;
   o->routed_scale = h->routed_scale;
   o->bias_selection_only = h->sel_only;
+  o->fp8_experts = h->fp8;
   return MOE_OK;
 }
 

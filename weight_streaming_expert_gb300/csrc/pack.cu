@@ -20,6 +20,13 @@
 //   down tile (e, sl), 8 rows: output rows 8sl .. 8sl + 7
 // 16-byte chunk (tile, q, lane) sits at ((tile * H/32 + q) * 32 + lane) for
 // gate/up (k = H) and ((tile * I/32 + q) * 32 + lane) for down (k = I).
+//
+// E4M3 codes (one byte each): tiles of 16 rows, the same bytes as 8 bf16
+// rows.  A tile is two n8 blocks; lane (g, t)'s 16-byte chunk q holds the
+// codes of block 0's row g at k = 32q + 8t .. +7, then those of block 1's:
+//   gate/up tile (e, tt), block b: n even -> gate row 8tt + 4b + n/2,
+//                                  n odd  -> up row   8tt + 4b + n/2
+//   down slab (e, sl), block b: output rows 16sl + 8b .. 16sl + 8b + 7
 #include "kernels.cuh"
 
 namespace wse {
@@ -62,6 +69,49 @@ __global__ void pack_down_kernel(const uint4* __restrict__ src, uint4* __restric
   }
 }
 
+__global__ void pack_gate_up_fp8_kernel(const uint2* __restrict__ src, uint4* __restrict__ dst, int E, int I,
+                                        int H) {
+  const int KC = H / 32, TPG = 2 * I / 16, RC = H / 8;  // RC: 8-byte chunks per source row
+  const long long total = (long long)E * TPG * KC * 32;
+  for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < total;
+       c += (long long)gridDim.x * blockDim.x) {
+    const int lane = (int)(c & 31);
+    long long r = c >> 5;
+    const int q = (int)(r % KC);
+    r /= KC;
+    const int tt = (int)(r % TPG);
+    const long long e = r / TPG;
+    const int g = lane >> 2, t = lane & 3;
+    uint2 v[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int ri = 8 * tt + 4 * b + (g >> 1);
+      const int row = (g & 1) ? I + ri : ri;
+      v[b] = src[((size_t)e * 2 * I + row) * RC + 4 * q + t];
+    }
+    dst[c] = make_uint4(v[0].x, v[0].y, v[1].x, v[1].y);
+  }
+}
+
+__global__ void pack_down_fp8_kernel(const uint2* __restrict__ src, uint4* __restrict__ dst, int E, int H,
+                                     int I) {
+  const int KC = I / 32, SL = H / 16, RC = I / 8;
+  const long long total = (long long)E * SL * KC * 32;
+  for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < total;
+       c += (long long)gridDim.x * blockDim.x) {
+    const int lane = (int)(c & 31);
+    long long r = c >> 5;
+    const int q = (int)(r % KC);
+    r /= KC;
+    const int sl = (int)(r % SL);
+    const long long e = r / SL;
+    const int g = lane >> 2, t = lane & 3;
+    const uint2 v0 = src[((size_t)e * H + 16 * sl + g) * RC + 4 * q + t];
+    const uint2 v1 = src[((size_t)e * H + 16 * sl + 8 + g) * RC + 4 * q + t];
+    dst[c] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+  }
+}
+
 }  // namespace
 
 void pack_gate_up(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int I, int H,
@@ -73,6 +123,16 @@ void pack_gate_up(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int I, in
 void pack_down(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int H, int I, cudaStream_t s) {
   pack_down_kernel<<<4096, 256, 0, s>>>(reinterpret_cast<const uint4*>(src),
                                         reinterpret_cast<uint4*>(dst), E, H, I);
+}
+
+void pack_gate_up_fp8(const uint8_t* src, uint8_t* dst, int E, int I, int H, cudaStream_t s) {
+  pack_gate_up_fp8_kernel<<<4096, 256, 0, s>>>(reinterpret_cast<const uint2*>(src), reinterpret_cast<uint4*>(dst),
+                                               E, I, H);
+}
+
+void pack_down_fp8(const uint8_t* src, uint8_t* dst, int E, int H, int I, cudaStream_t s) {
+  pack_down_fp8_kernel<<<4096, 256, 0, s>>>(reinterpret_cast<const uint2*>(src), reinterpret_cast<uint4*>(dst),
+                                            E, H, I);
 }
 
 }  // namespace wse

@@ -56,6 +56,35 @@ class MoELayer:
             raise N.MoEError("moe_create", N.MOE_ERR_INVALID_ARG, N.last_error())
         self._h = ctypes.c_void_p(h)
 
+    @classmethod
+    def fp8(cls, w_router, q_gate_up, s_gate_up, q_down, s_down, topk: int):
+        """A layer with fp8 (E4M3) expert weights and fp32 per-row scales
+        (``moe_create_fp8``): w_router bf16 [E,H]; q_gate_up uint8 [E,2I,H],
+        s_gate_up fp32 [E,2I]; q_down uint8 [E,H,I], s_down fp32 [E,H]."""
+        E, H = w_router.shape
+        I = q_down.shape[2]
+        if w_router.dtype != torch.bfloat16 or q_gate_up.dtype != torch.uint8 or q_down.dtype != torch.uint8:
+            raise ValueError("w_router must be bf16 and the codes uint8")
+        if s_gate_up.dtype != torch.float32 or s_down.dtype != torch.float32:
+            raise ValueError("the row scales must be fp32")
+        for t in (w_router, q_gate_up, s_gate_up, q_down, s_down):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("weights must be contiguous CUDA tensors")
+        if (tuple(q_gate_up.shape) != (E, 2 * I, H) or tuple(q_down.shape) != (E, H, I)
+                or tuple(s_gate_up.shape) != (E, 2 * I) or tuple(s_down.shape) != (E, H)):
+            raise ValueError("shapes must be [E,2I,H], [E,2I], [E,H,I], [E,H]")
+        self = cls.__new__(cls)
+        self.hidden, self.n_experts, self.topk, self.inter = H, E, topk, I
+        self.shared = False
+        self.device = w_router.device
+        with torch.cuda.device(self.device):
+            h = N.lib().moe_create_fp8(H, E, topk, I, _ptr(w_router), _ptr(q_gate_up), _ptr(s_gate_up),
+                                       _ptr(q_down), _ptr(s_down))
+        if not h:
+            raise N.MoEError("moe_create_fp8", N.MOE_ERR_INVALID_ARG, N.last_error())
+        self._h = ctypes.c_void_p(h)
+        return self
+
     @property
     def handle(self):
         return self._h

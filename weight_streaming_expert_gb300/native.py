@@ -41,7 +41,8 @@ class moe_info_t(ctypes.Structure):
                 ("weight_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
                 ("kernels_per_forward", ctypes.c_int), ("router_split", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("shared_expert", ctypes.c_int),
-                ("routed_scale", ctypes.c_float), ("bias_selection_only", ctypes.c_int)]
+                ("routed_scale", ctypes.c_float), ("bias_selection_only", ctypes.c_int),
+                ("fp8_experts", ctypes.c_int)]
 
 
 class moe_layer_opts_t(ctypes.Structure):
@@ -79,6 +80,8 @@ def lib(build_if_missing: bool = True):
         L.moe_create.restype = vp
         L.moe_create_ex.argtypes = [ci, ci, ci, ci, vp, vp, vp, ctypes.POINTER(moe_layer_opts_t)]
         L.moe_create_ex.restype = vp
+        L.moe_create_fp8.argtypes = [ci, ci, ci, ci, vp, vp, vp, vp, vp]
+        L.moe_create_fp8.restype = vp
         L.moe_forward.argtypes = [vp, vp, vp, vp, ci, vp]
         L.moe_forward.restype = ci
         L.moe_forward_ex.argtypes = [vp, vp, vp, vp, vp, ci, vp, cu]
