@@ -154,6 +154,7 @@ moe_layer_t* moe_create_ex(int hidden, int n_experts, int topk, int inter,
  *   w_router   device bf16 [E][H] (16-byte aligned).
  *   q_gate_up  device uint8 [E][2I][H] E4M3 codes (gate rows first), 16-byte
  *              aligned;      s_gate_up device fp32 [E][2I], 4-byte aligned.
+ *              Codes must be finite (not S.1111.111, E4M3's NaN).
  *   q_down     device uint8 [E][H][I] E4M3 codes, 16-byte aligned;
  *              s_down     device fp32 [E][H], 4-byte aligned.
  * hidden, n_experts, topk, inter as moe_create.  The codes and scales are
