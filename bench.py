@@ -65,8 +65,10 @@ def source_hash(paths):
 LAYER_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
                  for f in ("layer_kernel.cuh", "routing.cuh", "common.cuh", "kernels.cuh",
                            "layer_kernel_a.cu", "layer_kernel_b.cu", "layer_kernel_c.cu", "layer_kernel_d.cu",
-                           "layer_kernel_e.cu", "layer_kernel_f.cu")]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "layer_traffic.json")
+                           "layer_kernel_e.cu", "layer_kernel_f.cu", "layer_kernel_g.cu", "layer_kernel_h.cu")]
+# DRAM traffic records of one ncu capture each: bf16 and fp8 expert weights
+TRAFFIC_FILES = {False: os.path.join(ROOT, "profiles", "layer_traffic.json"),
+                 True: os.path.join(ROOT, "profiles", "layer_traffic_fp8.json")}
 
 
 def measured_peaks():
@@ -383,26 +385,53 @@ def time_e2e(wkl, steps):
     return us, M * H * 2, M * H * 2 + M * k * 4
 
 
-def oracle_call_us(shape, M, zipf, budget_s, host=None, max_calls=None):
-    """Mean wall time of the CPU oracle on one layer call, timed on samples of
-    ONE token each (the oracle's work is linear in M, so a call costs M of
-    them).  Returns (us_per_call, n_samples, host_weights)."""
+ORACLE_FN = {"plain": "moe_forward", "variant": "moe_forward (shared expert, routed scale 2.5, selection-only bias)",
+             "fp8": "moe_forward_fp8"}
+
+
+def oracle_layer(shape, kind):
+    """The oracle call of one token on the timed workload's first layer
+    (weight seed 1000; the variant's shared expert from seed 1500, as the
+    Workload builds it): kind "plain", "variant" or "fp8"."""
+    import torch
     from oracle.oracle import Oracle
     from weight_streaming_expert_gb300 import workloads as wl
     orc = Oracle()
-    if host is None:
-        w_r, w_gu, w_d = wl.layer_weights(shape, seed=1000, device="cuda" if _has_cuda() else "cpu")
-        host = (wl.bf16_bits(w_r), wl.bf16_bits(w_gu), wl.bf16_bits(w_d))
-        del w_r, w_gu, w_d
+    dev = "cuda" if _has_cuda() else "cpu"
+    if kind == "fp8":
+        w_r, q_gu, s_gu, q_d, s_d = wl.fp8_expert_weights(shape, seed=1000, device=dev)
+        h = (wl.bf16_bits(w_r), q_gu.cpu().numpy(), s_gu.cpu().numpy(), q_d.cpu().numpy(), s_d.cpu().numpy())
+        return lambda x, bias: orc.moe_forward_fp8(x, *h, shape.topk, bias=bias)
+    w_r, w_gu, w_d = wl.layer_weights(shape, seed=1000, device=dev)
+    h = (wl.bf16_bits(w_r), wl.bf16_bits(w_gu), wl.bf16_bits(w_d))
+    kw = {}
+    if kind == "variant":
+        g = torch.Generator(device=dev).manual_seed(1500)
+        H, I = shape.hidden, shape.inter
+        kw = dict(shared_gate_up=wl.bf16_bits((torch.randn(2 * I, H, generator=g, device=dev) * wl.WEIGHT_STD)
+                                              .to(torch.bfloat16)),
+                  shared_down=wl.bf16_bits((torch.randn(H, I, generator=g, device=dev) * wl.WEIGHT_STD)
+                                           .to(torch.bfloat16)),
+                  routed_scale=2.5, bias_selection_only=True)
+    return lambda x, bias: orc.moe_forward(x, *h, shape.topk, bias=bias, **kw)
+
+
+def oracle_call_us(shape, M, zipf, budget_s, call=None, max_calls=None, kind="plain"):
+    """Mean wall time of the CPU oracle on one layer call, timed on samples of
+    ONE token each (the oracle's work is linear in M, so a call costs M of
+    them).  Returns (us_per_call, n_samples, call)."""
+    from weight_streaming_expert_gb300 import workloads as wl
+    if call is None:
+        call = oracle_layer(shape, kind)
     bias = wl.zipf_router_bias(shape.n_experts).numpy() if zipf else None
     xs = [wl.bf16_bits(wl.tokens(1, shape.hidden, seed=1_000_000 + i)) for i in range(64)]
-    orc.moe_forward(xs[0], *host, shape.topk, bias=bias)     # warm caches
+    call(xs[0], bias)     # warm caches
     times = []
     t_start = time.perf_counter()
     i = 0
     while True:
         t0 = time.perf_counter()
-        orc.moe_forward(xs[i % len(xs)], *host, shape.topk, bias=bias)
+        call(xs[i % len(xs)], bias)
         times.append(time.perf_counter() - t0)
         i += 1
         if max_calls is not None and i >= max_calls:
@@ -410,7 +439,22 @@ def oracle_call_us(shape, M, zipf, budget_s, host=None, max_calls=None):
         if time.perf_counter() - t_start > budget_s and i >= 3:
             break
     per_token = statistics.mean(times)
-    return per_token * M * 1e6, len(times), host
+    return per_token * M * 1e6, len(times), call
+
+
+def workload_name(args, shape, M):
+    """The timed workload, named by what it is (both arms)."""
+    return (f"Ling-shaped MoE {'block-verify' if M >= 16 else 'verify' if M > 1 else 'decode'} step"
+            f"{' (per-GPU slice of a 4-way TP split)' if args.shape == 'ling_tp4' else ''}: "
+            f"hidden {shape.hidden}, {shape.n_experts} experts, top-{shape.topk} softmax+renorm, "
+            f"SwiGLU inter {shape.inter}, "
+            f"{'+ shared expert, routed scale 2.5, bias for selection only, ' if args.variant else ''}"
+            f"{'fp8 E4M3 expert weights with fp32 row scales, ' if args.fp8 else ''}"
+            f"M={M}, {'Zipf(1.1) router bias' if args.zipf else 'uniform routing'}")
+
+
+def oracle_kind(args):
+    return "fp8" if args.fp8 else "variant" if args.variant else "plain"
 
 
 def _has_cuda():
@@ -446,11 +490,13 @@ def run_ours(args):
     alone_us = float(time_kernel_alone(wkl, min(256, max(16, args.steps))).mean() * 1000.0)
     phases = phase_breakdown(wkl)
     traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        with open(TRAFFIC_FILE) as f:
+    traffic_file = TRAFFIC_FILES[bool(args.fp8)]
+    if os.path.exists(traffic_file):
+        with open(traffic_file) as f:
             tr = json.load(f)
         if (tr.get("source_hash") == source_hash(LAYER_SOURCES) and tr.get("M") == M
-                and args.shape == tr.get("shape", "ling") and not args.variant and not args.fp8):
+                and args.shape == tr.get("shape", "ling") and not args.variant
+                and bool(tr.get("fp8", False)) == bool(args.fp8)):
             # measured on a smaller run (one layer, 8 calls): DRAM traffic
             # follows the algorithmic bytes, so scale it to this run's launches
             traffic = int(round(tr["bytes_per_launch"] * bytes_call / tr["algorithmic_bytes_per_launch"]))
@@ -476,9 +522,10 @@ def run_ours(args):
     if not args.no_cpu_baseline and rank == 0:
         wkl.close()
         torch.cuda.empty_cache()
-        us_cpu, n, _ = oracle_call_us(shape, M, args.zipf, args.cpu_budget)
+        kind = oracle_kind(args)
+        us_cpu, n, _ = oracle_call_us(shape, M, args.zipf, args.cpu_budget, kind=kind)
         cpu = {"value": round(us_cpu, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} single-token calls of the CPU oracle on layer seed 1000 "
+               "sample": f"{n} single-token calls of the CPU oracle's {ORACLE_FN[kind]} on layer seed 1000 "
                          f"(x seeds 1e6+i), mean x M={M}; single-threaded C++"}
     else:
         wkl.close()
@@ -488,13 +535,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8 weights, bf16 tokens" if args.fp8 else "bf16",
             "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens (random init, no checkpoint)",
-            "config": {"workload": f"Ling-shaped MoE {'block-verify' if M >= 16 else 'verify' if M > 1 else 'decode'} step"
-                                   f"{' (per-GPU slice of a 4-way TP split)' if args.shape == 'ling_tp4' else ''}: "
-                                   f"hidden {shape.hidden}, {shape.n_experts} experts, top-{shape.topk} softmax+renorm, "
-                                   f"SwiGLU inter {shape.inter}, "
-                                   f"{'+ shared expert, routed scale 2.5, bias for selection only, ' if args.variant else ''}"
-                                   f"{'fp8 E4M3 expert weights with fp32 row scales, ' if args.fp8 else ''}"
-                                   f"M={M}, {'Zipf(1.1) router bias' if args.zipf else 'uniform routing'}",
+            "config": {"workload": workload_name(args, shape, M),
                        "M": M, "layers_cycled": n_layers, "x_pool": args.pool,
                        "l2_policy": f"inputs larger than L2: {n_layers} distinct layer weight sets cycled, "
                                     f"fresh x per call; L2 {l2 // (1024 * 1024)} MiB",
@@ -531,22 +572,22 @@ def run_reference(args):
     shape = wl.SHAPES[args.shape]
     budget = args.cpu_budget
     # warmup samples (untimed), then timed samples bounded by the budget
-    us_w, _, host = oracle_call_us(shape, args.M, args.zipf, budget_s=0.0,
-                                   max_calls=max(1, min(args.warmup, 3)))
-    us, n, _ = oracle_call_us(shape, args.M, args.zipf, budget_s=budget, host=host,
+    kind = oracle_kind(args)
+    us_w, _, call = oracle_call_us(shape, args.M, args.zipf, budget_s=0.0,
+                                   max_calls=max(1, min(args.warmup, 3)), kind=kind)
+    us, n, _ = oracle_call_us(shape, args.M, args.zipf, budget_s=budget, call=call,
                               max_calls=max(1, args.steps))
     cores = 1
     line = {
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 0,
         "steps": n, "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate over bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 accumulate over E4M3 x row scale" if args.fp8 else "f32 accumulate over bf16",
         "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens",
-        "config": {"workload": f"Ling-shaped MoE step: hidden {shape.hidden}, {shape.n_experts} experts, "
-                               f"top-{shape.topk}, inter {shape.inter}, M={args.M}",
-                   "M": args.M},
+        "config": {"workload": workload_name(args, shape, args.M), "M": args.M},
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{n} single-token oracle calls (of {args.steps} requested steps, "
-                                   f"bounded to {budget:.0f} s), mean x M={args.M}"},
+                         "sample": f"{n} single-token calls of the oracle's {ORACLE_FN[kind]} (of {args.steps} "
+                                   f"requested steps, bounded to {budget:.0f} s), mean x M={args.M}"},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -235,8 +235,11 @@ typedef struct {
   int hidden, n_experts, topk, inter;
   int max_tokens;          /* MOE_MAX_TOKENS */
   int n_sms;               /* SMs of the device the handle lives on */
-  int gateup_stages;       /* shared-memory ring depth of the gate/up phase */
-  int down_stages;         /* shared-memory stages of the down phase */
+  int gateup_stages;       /* shared-memory ring depth of the gate/up phase
+                              (the ring of a call at M = 64: an fp8 layer's
+                              calls with M <= 8 run a second instance with a
+                              smaller reduction area and deeper rings) */
+  int down_stages;         /* shared-memory stages of the down phase (M = 64) */
   int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 bf16 or
                               16 fp8 rows x H) */
   int down_tile_bytes;     /* bytes of one down super tile (8 slabs of

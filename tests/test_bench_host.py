@@ -49,10 +49,14 @@ def test_call_bytes_count_router_and_io_once():
     assert bench.algorithmic_bytes(2560, 512, 8, 512, M=6, n_active=46) - base == 46 * 3 * 2560 * 512 * 2
 
 
-def test_traffic_record_is_complete_and_near_the_algorithmic_bytes():
-    # the committed ncu record the bench scales into roofline.traffic
-    with open(bench.TRAFFIC_FILE) as f:
+@pytest.mark.parametrize("fp8", [False, True])
+def test_traffic_record_is_complete_and_near_the_algorithmic_bytes(fp8):
+    # the committed ncu records the bench scales into roofline.traffic
+    if not os.path.exists(bench.TRAFFIC_FILES[fp8]):
+        pytest.skip("no record for this weight type")
+    with open(bench.TRAFFIC_FILES[fp8]) as f:
         tr = json.load(f)
+    assert bool(tr.get("fp8", False)) == fp8
     for key in ("source_hash", "shape", "M", "bytes_per_launch", "algorithmic_bytes_per_launch", "launches", "command"):
         assert key in tr
     reads = [l["dram_read"] + l["dram_write"] for l in tr["launches"]]

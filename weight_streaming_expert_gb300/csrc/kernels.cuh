@@ -38,12 +38,14 @@ struct LayerArgs {
 // layer_smem_bytes(ring_bytes, NP, buckets).  KPW = H/256.
 using LayerKernel = void (*)(LayerArgs);
 // variant: the instance that handles the layer variants; fp8: the instance
-// for E4M3 expert weights (plain layers only).  nullptr: no such instance.
-LayerKernel layer_kernel_for(int kpw, bool variant, bool fp8 = false);
+// for E4M3 expert weights (plain layers only) whose groups hold up to
+// 8 x token_blocks tokens (1: calls with M <= 8; 2: any call).  nullptr: no
+// such instance.
+LayerKernel layer_kernel_for(int kpw, bool variant, bool fp8 = false, int token_blocks = 2);
 size_t layer_smem_bytes(uint32_t ring_bytes, int NP, int E);
-// Bytes of the reduction area that follows the gate/up stages (fp8 tiles
-// hold two n8 blocks: twice the partials).
-uint32_t layer_reduction_bytes(bool fp8 = false);
+// Bytes of the reduction area that follows the gate/up stages (fp8 with two
+// token blocks: two partials per lane).
+uint32_t layer_reduction_bytes(bool fp8 = false, int token_blocks = 2);
 
 // Create-time re-layout (pack.cu).
 void pack_gate_up(const __nv_bfloat16* src, __nv_bfloat16* dst, int E, int I, int H,

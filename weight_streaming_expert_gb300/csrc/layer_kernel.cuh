@@ -172,8 +172,14 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g));
 // FP8: expert weights as E4M3 codes with fp32 per-row scales -- tiles of 16
 // rows (the same bytes as 8 bf16 rows), codes converted to f16 in registers,
 // tokens and h converted to f16 per group, the row scales applied in fp32
-// after the sums (reducer and down epilogue).
-template <int KPW, bool VARIANT, bool FP8>
+// after the sums (reducer and down epilogue).  TB = 1 serves groups of at
+// most 8 tokens (calls with M <= 8): the weights are the MMA's A operand
+// (its 16 rows are the tile's two 8-row blocks) and the tokens one n8 B
+// block -- two MMAs per 16-byte chunk and one set of token registers.
+// TB = 2 serves groups of up to 16: the 16 tokens are A and each 8-row
+// block of the tile a B operand (four MMAs per chunk).  bf16 weights: tokens
+// are A, the 8-row tile B; TB is unused.
+template <int KPW, bool VARIANT, bool FP8, int TB>
 __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs a) {
   using namespace layer_detail;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -182,7 +188,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   const int S = a.gu_stages;
   constexpr int GU_ROWS = FP8 ? 16 : kGateUpTileRows;  // weight rows per gate/up tile
   constexpr int D_ROWS = FP8 ? 16 : kDownTileRows;     // output rows per down slab
-  constexpr int NB = FP8 ? 2 : 1;                      // n8 blocks per tile (partials per lane)
+  static_assert(TB == 1 || TB == 2, "token blocks");
+  constexpr bool WA = FP8 && TB == 1;                  // the weights are the MMA's A operand
+  constexpr int NB = FP8 && TB == 2 ? 2 : 1;           // float4 partials per lane (gate/up reduction)
   const int NSL = kConsumerWarps, SD = a.d_stages;  // slabs per down super tile, down slots
   const int MK = a.M * a.K;                     // routed pairs (token * K + slot)
   const bool shared = VARIANT && a.shared;
@@ -554,6 +562,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   {
     // ---- 4. gate/up + SwiGLU
     uint4 xa[KPW], xb[KPW];  // token rows g4 and g4 + 8 of the group: this warp's k chunks
+                             // (weights as A: row g4 only)
     int cur_g = -1, start = 0, cnt = 0;
     // this CTA's statically split tiles come first: after the last of them
     // (or at once if it has none) the warp reports them reduced
@@ -584,22 +593,27 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
 #pragma unroll
         for (int q = 0; q < KPW; ++q) {
           xa[q] = x0[4 * (warp * KPW + q)];
-          xb[q] = x1[4 * (warp * KPW + q)];
+          if constexpr (!WA) xb[q] = x1[4 * (warp * KPW + q)];
           if constexpr (FP8) {
             xa[q] = bf16x8_to_f16x8(xa[q]);
-            xb[q] = bf16x8_to_f16x8(xb[q]);
+            if constexpr (!WA) xb[q] = bf16x8_to_f16x8(xb[q]);
           }
         }
         cur_g = g;
       }
-      float2 sc[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};  // (gate, up) row scales per block
+      // fp8 row scales, loaded early by this tile's reducer: weights as A,
+      // (gate, up) of intermediate row 8 tt + g4 in (sg.x, su.x); weights as
+      // B, rows 8 tt + 2 t4 and + 1 in (sg.x, sg.y) and (su.x, su.y)
+      float2 sg = make_float2(1.f, 1.f), su = make_float2(1.f, 1.f);
       if constexpr (FP8) {
-        if (warp == (j & (kRedSlots - 1))) {  // this tile's reducer: its rows' scales, early
-          const float* sg = a.s_gu + (size_t)rt.grp_expert[g] * 2 * a.I;
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const int r = 8 * tt + 4 * b + t4;
-            sc[b] = make_float2(__ldg(sg + r), __ldg(sg + a.I + r));
+        if (warp == (j & (kRedSlots - 1))) {
+          const float* sp = a.s_gu + (size_t)rt.grp_expert[g] * 2 * a.I + 8 * tt + (WA ? g4 : 2 * t4);
+          if constexpr (WA) {
+            sg.x = __ldg(sp);
+            su.x = __ldg(sp + a.I);
+          } else {
+            sg = __ldg(reinterpret_cast<const float2*>(sp));
+            su = __ldg(reinterpret_cast<const float2*>(sp + a.I));
           }
         }
       }
@@ -608,14 +622,23 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         break;
       }
       if (j == 0 && tid == 0) stamp(a, 4);
-      // bf16: c0, c1 = the two k-steps of the one n8 block; fp8: c0, c1 = the
-      // two n8 blocks, each over both k-steps
+      // bf16: c0, c1 = the two k-steps of the one n8 block.  fp8 with weights
+      // as A: c0, c1 = the two k-steps; weights as B: c0 = the gate block,
+      // c1 = the up block, each over both k-steps
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const uint4* wp = reinterpret_cast<const uint4*>(ring + (size_t)s * a.gu_tile) + (warp * KPW) * 32 + lane;
 #pragma unroll
       for (int q = 0; q < KPW; ++q) {
         const uint4 b = wp[q * 32];
-        if constexpr (FP8) {  // b.x, b.y: block 0 row g4 (8 codes); b.z, b.w: block 1 row g4
+        if constexpr (WA) {  // b.x, b.y: gate row 8 tt + g4 (8 codes); b.z, b.w: up row 8 tt + g4
+          uint32_t g0, g1, g2, g3, u0, u1, u2, u3;
+          e4m3x4_to_f16x2(b.x, g0, g1);
+          e4m3x4_to_f16x2(b.y, g2, g3);
+          e4m3x4_to_f16x2(b.z, u0, u1);
+          e4m3x4_to_f16x2(b.w, u2, u3);
+          mma_f16(c0, g0, u0, g1, u1, xa[q].x, xa[q].y);
+          mma_f16(c1, g2, u2, g3, u3, xa[q].z, xa[q].w);
+        } else if constexpr (FP8) {  // the same codes, as the B columns of the gate and up blocks
           uint32_t f0, f1, f2, f3;
           e4m3x4_to_f16x2(b.x, f0, f1);
           e4m3x4_to_f16x2(b.y, f2, f3);
@@ -634,7 +657,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       if (lane == 0) mbar_arrive(empty(s));  // stage free for the producer
 
       const int slot = j & (kRedSlots - 1);
-      if constexpr (FP8) {
+      if constexpr (NB == 2) {
         red[((slot * kConsumerWarps + warp) * 32 + lane) * NB] = make_float4(c0[0], c0[1], c0[2], c0[3]);
         red[((slot * kConsumerWarps + warp) * 32 + lane) * NB + 1] = make_float4(c1[0], c1[1], c1[2], c1[3]);
       } else {
@@ -648,29 +671,46 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
           record_timeout(a.ws, 2, kErrTimeoutReduce, j, S, redbar(slot), waited);
           break;
         }
+        float4 acc[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          float4 acc = red[((slot * kConsumerWarps) * 32 + lane) * NB + b];
+          acc[b] = red[((slot * kConsumerWarps) * 32 + lane) * NB + b];
 #pragma unroll
           for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
             const float4 v = red[((slot * kConsumerWarps + w2) * 32 + lane) * NB + b];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            acc[b].x += v.x;
+            acc[b].y += v.y;
+            acc[b].z += v.z;
+            acc[b].w += v.w;
           }
-          // (acc.x, acc.y) = (gate, up) of group token g4, intermediate row
-          // GU_ROWS/2 tt + 4 b + t4; (acc.z, acc.w) the same for token g4 + 8
-          const int r = (GU_ROWS / 2) * tt + 4 * b + t4;
-          if constexpr (FP8) {  // the row scales, after the sums
-            acc.x *= sc[b].x;
-            acc.z *= sc[b].x;
-            acc.y *= sc[b].y;
-            acc.w *= sc[b].y;
-          }
-          if (g4 < cnt) a.ws.h[(size_t)(start + g4) * a.I + r] = __float2bfloat16_rn(silu(acc.x) * acc.y);
+        }
+        // the row scales after the sums, then SwiGLU and ONE bf16 rounding
+        if constexpr (WA) {
+          // (x, y) = gate of intermediate row 8 tt + g4 for group tokens 2 t4,
+          // 2 t4 + 1; (z, w) = up of the same row and tokens
+          const int r = 8 * tt + g4, n = 2 * t4;
+          const float4 v = acc[0];
+          if (n < cnt) a.ws.h[(size_t)(start + n) * a.I + r] = __float2bfloat16_rn(silu(sg.x * v.x) * (su.x * v.z));
+          if (n + 1 < cnt)
+            a.ws.h[(size_t)(start + n + 1) * a.I + r] = __float2bfloat16_rn(silu(sg.x * v.y) * (su.x * v.w));
+        } else if constexpr (FP8) {
+          // gate acc[0], up acc[1]: (x, y) = group token g4, intermediate rows
+          // 8 tt + 2 t4 and + 1; (z, w) = token g4 + 8
+          const int r = 8 * tt + 2 * t4;
+          const float4 gt = acc[0], up = acc[1];
+          if (g4 < cnt)
+            *reinterpret_cast<__nv_bfloat162*>(a.ws.h + (size_t)(start + g4) * a.I + r) = __floats2bfloat162_rn(
+                silu(sg.x * gt.x) * (su.x * up.x), silu(sg.y * gt.y) * (su.y * up.y));
           if (g4 + 8 < cnt)
-            a.ws.h[(size_t)(start + g4 + 8) * a.I + r] = __float2bfloat16_rn(silu(acc.z) * acc.w);
+            *reinterpret_cast<__nv_bfloat162*>(a.ws.h + (size_t)(start + g4 + 8) * a.I + r) = __floats2bfloat162_rn(
+                silu(sg.x * gt.z) * (su.x * up.z), silu(sg.y * gt.w) * (su.y * up.w));
+        } else {
+          // (x, y) = (gate, up) of group token g4, intermediate row 4 tt + t4;
+          // (z, w) the same for token g4 + 8
+          const int r = (GU_ROWS / 2) * tt + t4;
+          const float4 v = acc[0];
+          if (g4 < cnt) a.ws.h[(size_t)(start + g4) * a.I + r] = __float2bfloat16_rn(silu(v.x) * v.y);
+          if (g4 + 8 < cnt) a.ws.h[(size_t)(start + g4 + 8) * a.I + r] = __float2bfloat16_rn(silu(v.z) * v.w);
         }
       }
       if (j == n_static - 1) {  // every static tile of this warp's share is reduced
@@ -691,9 +731,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     // ---- 5. down GEMV, weighted rows y[pair] = w_pair * (W_d h_pair);
     // warp w takes slab w of every super tile
     const int kpd = a.I / 32;  // 32-wide k chunks of a down row (<= kMaxDownChunks)
-    uint4 ha[kMaxDownChunks], hb[kMaxDownChunks];
-    int pid0 = -1, pid1 = -1;
-    float pw0 = 0.f, pw1 = 0.f;
+    uint4 ha[kMaxDownChunks], hb[kMaxDownChunks];  // h rows of group tokens g4, g4 + 8 (weights as A: g4)
+    // the pairs this lane stores: weights as A, group tokens 2 t4 and
+    // 2 t4 + 1; otherwise tokens g4 and g4 + 8
+    int pid[2] = {-1, -1};
+    float pw[2] = {0.f, 0.f};
     int cur_g = -1, cur_de = 0;
     for (int j = 0;; ++j) {
       const int s = j % SD;
@@ -716,33 +758,43 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         for (int q = 0; q < kMaxDownChunks; ++q) {
           if (q < kpd) {
             ha[q] = __ldcg(h0 + 4 * q);  // written by other SMs in this grid: L2, not L1
-            hb[q] = __ldcg(h1 + 4 * q);
+            if constexpr (!WA) hb[q] = __ldcg(h1 + 4 * q);
             if constexpr (FP8) {
               ha[q] = bf16x8_to_f16x8(ha[q]);
-              hb[q] = bf16x8_to_f16x8(hb[q]);
+              if constexpr (!WA) hb[q] = bf16x8_to_f16x8(hb[q]);
             }
           }
         }
         if constexpr (FP8) cur_de = rt.grp_expert[g];
-        pid0 = g4 < cnt ? rt.pair_list[start + g4] : -1;
-        pid1 = g4 + 8 < cnt ? rt.pair_list[start + g4 + 8] : -1;
-        pw0 = pid0 >= 0 ? rt.s_w[pid0] : 0.f;
-        pw1 = pid1 >= 0 ? rt.s_w[pid1] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int n = WA ? 2 * t4 + i : g4 + 8 * i;
+          pid[i] = n < cnt ? rt.pair_list[start + n] : -1;
+          pw[i] = pid[i] >= 0 ? rt.s_w[pid[i]] : 0.f;
+        }
         cur_g = g;
       }
-      float2 rs[NB];  // fp8: the output rows' scales, loaded while the data lands
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        rs[b] = make_float2(1.f, 1.f);
-        if constexpr (FP8)
-          rs[b] = __ldg(reinterpret_cast<const float2*>(a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + 8 * b + 2 * t4));
+      // fp8 scales of the output rows, loaded while the data lands: weights
+      // as A, rows 16 sl + g4 and + 8 in (rs.x, rs.y); as B, rows
+      // 16 sl + 8 b + 2 t4 and + 1 of block b in (rs.x, rs.y) and (rs.z, rs.w)
+      float4 rs = make_float4(1.f, 1.f, 1.f, 1.f);
+      if constexpr (WA) {
+        const float* sd = a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + g4;
+        rs.x = __ldg(sd);
+        rs.y = __ldg(sd + 8);
+      } else if constexpr (FP8) {
+        const float* sd = a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + 2 * t4;
+        const float2 r0 = __ldg(reinterpret_cast<const float2*>(sd));
+        const float2 r1 = __ldg(reinterpret_cast<const float2*>(sd + 8));
+        rs = make_float4(r0.x, r0.y, r1.x, r1.y);
       }
       if (!warp_wait(dfull(s), ph, &waited)) {
         record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dfull(s), waited);
         break;
       }
       if (j == 0 && tid == 0) stamp(a, 14);
-      // bf16: c0, c1 = the two k-steps; fp8: c0, c1 = the two n8 blocks
+      // bf16 and fp8 with weights as A: c0, c1 = the two k-steps; fp8 with
+      // weights as B: c0, c1 = the slab's two 8-row blocks
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const uint4* bp =
           reinterpret_cast<const uint4*>(ring + (size_t)cell_tab[s * kConsumerWarps + warp] * a.d_tile) + lane;
@@ -750,7 +802,15 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       for (int q = 0; q < kMaxDownChunks; ++q) {
         if (q < kpd) {
           const uint4 b = bp[q * 32];
-          if constexpr (FP8) {  // b.x, b.y: output row g4 of block 0; b.z, b.w: of block 1
+          if constexpr (WA) {  // b.x, b.y: output row 16 sl + g4; b.z, b.w: row 16 sl + 8 + g4
+            uint32_t p0, p1, p2, p3, r0, r1, r2, r3;
+            e4m3x4_to_f16x2(b.x, p0, p1);
+            e4m3x4_to_f16x2(b.y, p2, p3);
+            e4m3x4_to_f16x2(b.z, r0, r1);
+            e4m3x4_to_f16x2(b.w, r2, r3);
+            mma_f16(c0, p0, r0, p1, r1, ha[q].x, ha[q].y);
+            mma_f16(c1, p2, r2, p3, r3, ha[q].z, ha[q].w);
+          } else if constexpr (FP8) {  // the same codes, as the B columns of the two blocks
             uint32_t f0, f1, f2, f3;
             e4m3x4_to_f16x2(b.x, f0, f1);
             e4m3x4_to_f16x2(b.y, f2, f3);
@@ -768,19 +828,39 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       }
       __syncwarp();  // every lane has read the stage
       if (lane == 0) mbar_arrive(dempty(s));
-      // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of block b of the slab)
+      if constexpr (WA) {
+        // c0 + c1: (rows 16 sl + g4 | 16 sl + 8 + g4) x (tokens 2 t4, 2 t4 + 1)
+        const int row = sl * D_ROWS + g4;
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int row = sl * D_ROWS + 8 * b + 2 * t4;
-        float v[4];  // (token g4 | g4 + 8) x (rows row, row + 1)
+        for (int i = 0; i < 2; ++i)
+          if (pid[i] >= 0) {
+            float* yr = a.ws.y + (size_t)pid[i] * a.H + row;
+            yr[0] = pw[i] * (rs.x * (c0[i] + c1[i]));
+            yr[8] = pw[i] * (rs.y * (c0[2 + i] + c1[2 + i]));
+          }
+      } else if constexpr (FP8) {
+        // block b: (token g4 | g4 + 8) x (rows 16 sl + 8 b + 2 t4, + 1)
+        const int row = sl * D_ROWS + 2 * t4;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = FP8 ? (b ? c1[i] : c0[i]) : c0[i] + c1[i];
-        if (pid0 >= 0)
-          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid0 * a.H + row) =
-              make_float2(pw0 * (rs[b].x * v[0]), pw0 * (rs[b].y * v[1]));
-        if (pid1 >= 0)
-          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid1 * a.H + row) =
-              make_float2(pw1 * (rs[b].x * v[2]), pw1 * (rs[b].y * v[3]));
+        for (int b = 0; b < 2; ++b) {
+          const float* v = b ? c1 : c0;
+          const float sx = b ? rs.z : rs.x, sy = b ? rs.w : rs.y;
+          if (pid[0] >= 0)
+            *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row + 8 * b) =
+                make_float2(pw[0] * (sx * v[0]), pw[0] * (sy * v[1]));
+          if (pid[1] >= 0)
+            *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row + 8 * b) =
+                make_float2(pw[1] * (sx * v[2]), pw[1] * (sy * v[3]));
+        }
+      } else {
+        // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of the slab)
+        const int row = sl * D_ROWS + 2 * t4;
+        if (pid[0] >= 0)
+          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row) =
+              make_float2(pw[0] * (c0[0] + c1[0]), pw[0] * (c0[1] + c1[1]));
+        if (pid[1] >= 0)
+          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row) =
+              make_float2(pw[1] * (c0[2] + c1[2]), pw[1] * (c0[3] + c1[3]));
       }
     }
     if (tid == 0) stamp(a, 7);

@@ -1,15 +1,15 @@
 // layer_kernel_a.cu -- layer kernel instances for hidden = 256 x {1,2,4,5}, plain
-// (one of six translation units compiled in parallel).
+// (one of eight translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {
 
 LayerKernel layer_kernel_plain_small(int kpw) {
   switch (kpw) {
-    case 1: return moe_layer_kernel<1, false, false>;
-    case 2: return moe_layer_kernel<2, false, false>;
-    case 4: return moe_layer_kernel<4, false, false>;
-    case 5: return moe_layer_kernel<5, false, false>;
+    case 1: return moe_layer_kernel<1, false, false, 2>;
+    case 2: return moe_layer_kernel<2, false, false, 2>;
+    case 4: return moe_layer_kernel<4, false, false, 2>;
+    case 5: return moe_layer_kernel<5, false, false, 2>;
     default: return nullptr;
   }
 }
@@ -18,6 +18,8 @@ size_t layer_smem_bytes(uint32_t ring_bytes, int NP, int E) {
   return layer_detail::kRingOff + (size_t)ring_bytes + routing_smem_bytes(NP, E);
 }
 
-uint32_t layer_reduction_bytes(bool fp8) { return layer_detail::kRedBytes * (fp8 ? 2u : 1u); }
+uint32_t layer_reduction_bytes(bool fp8, int token_blocks) {
+  return layer_detail::kRedBytes * (fp8 && token_blocks == 2 ? 2u : 1u);
+}
 
 }  // namespace wse

@@ -63,6 +63,16 @@ struct GraphEntry {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// One launch configuration of the layer kernel: the instance and its
+// shared-memory rings, sized for calls of up to max_tokens tokens.
+struct LayerPlan {
+  LayerKernel kernel = nullptr;
+  int max_tokens = 0;
+  int s_gu = 0, s_d = 0;    // gate/up ring depth, down stages
+  uint32_t ring_bytes = 0;
+  size_t smem_max = 0;      // dynamic shared memory at M = max_tokens
+};
+
 }  // namespace
 
 struct moe_layer {
@@ -84,10 +94,12 @@ struct moe_layer {
   size_t ws_bytes = 0, weight_bytes = 0;
   Workspace ws{};
   int ks = 1;               // hidden-dim split of the router matvec
-  int s_gu = 0, s_d = 0;    // gate/up ring depth, down stages
-  uint32_t tile_gu = 0, tile_d = 0, ring_bytes = 0;
-  size_t smem_max = 0;      // dynamic shared memory at M = MOE_MAX_TOKENS
-  LayerKernel kernel = nullptr;
+  uint32_t tile_gu = 0, tile_d = 0;
+  // plan[0] serves every M; an fp8 layer's plan[1] serves M <= 8 (groups of
+  // at most 8 tokens: one token block, half the reduction area)
+  LayerPlan plan[2];
+  int n_plans = 1;
+  const LayerPlan& plan_for(int M) const { return n_plans > 1 && M <= plan[1].max_tokens ? plan[1] : plan[0]; }
   std::map<int, GraphEntry> graphs;
   cudaStream_t cap_stream = nullptr;
 };
@@ -125,6 +137,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 // records are external event nodes when the stream is being captured.
 int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, int M,
                  cudaStream_t st, bool pdl, bool trace, cudaEvent_t* ev) {
+  const LayerPlan& pl = h->plan_for(M);
   LayerArgs la{};
   la.x = static_cast<const __nv_bfloat16*>(x);
   la.w_router = h->w_router;
@@ -138,11 +151,11 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   la.topk_w = tw;
   la.M = M; la.H = h->H; la.E = h->E; la.K = h->K; la.I = h->I;
   la.ks = h->ks;
-  la.gu_stages = h->s_gu;
-  la.d_stages = h->s_d;
+  la.gu_stages = pl.s_gu;
+  la.d_stages = pl.s_d;
   la.gu_tile = h->tile_gu;
   la.d_tile = h->tile_d;
-  la.ring_bytes = h->ring_bytes;
+  la.ring_bytes = pl.ring_bytes;
   la.trace = trace ? 1 : 0;
   la.shared = h->shared;
   la.routed_scale = h->routed_scale;
@@ -158,7 +171,7 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   c.numAttrs = pdl ? 1 : 0;
   c.gridDim = dim3(h->n_sms);
   c.blockDim = dim3(kExpertThreads);
-  c.dynamicSmemBytes = layer_smem_bytes(h->ring_bytes, M * h->kp(), h->ea());
+  c.dynamicSmemBytes = layer_smem_bytes(pl.ring_bytes, M * h->kp(), h->ea());
 
   cudaError_t e;
   unsigned ev_flags = cudaEventRecordDefault;
@@ -168,7 +181,7 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
     if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
   }
   if (ev && (e = cudaEventRecordWithFlags(ev[0], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = cudaLaunchKernelEx(&c, h->kernel, la)) != cudaSuccess) return cuda_fail(e, "layer kernel launch");
+  if ((e = cudaLaunchKernelEx(&c, pl.kernel, la)) != cudaSuccess) return cuda_fail(e, "layer kernel launch");
   if (ev && (e = cudaEventRecordWithFlags(ev[1], st, ev_flags)) != cudaSuccess) return cuda_fail(e, "event record");
   return MOE_OK;
 }
@@ -270,33 +283,38 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   h->fp8 = fp8 ? 1 : 0;
   h->dev = dev;
   h->n_sms = prop.multiProcessorCount;
-  h->kernel = layer_kernel_for(hidden / 256, variant, fp8);
   h->tile_gu = (uint32_t)(kGateUpTileRows * hidden * 2);
   h->tile_d = (uint32_t)(kDownTileRows * inter * 2);
   h->ks = gemv_split(hidden, n_experts, h->n_sms);
 
-  // Ring sized for the largest call (M = MOE_MAX_TOKENS): the gate/up stages
-  // plus the reduction area behind them, and the down stages over the same
-  // bytes, take what the opt-in shared memory leaves after the routing area
-  // (one CTA per SM; deep rings keep enough bytes in flight to cover the
-  // loaded HBM latency).
+  // Rings sized for the largest call of each plan: the gate/up stages plus
+  // the reduction area behind them, and the down stages over the same bytes,
+  // take what the opt-in shared memory leaves after the routing area (one
+  // CTA per SM; deep rings keep enough bytes in flight to cover the loaded
+  // HBM latency).  The down phase reuses the ring as slab-sized cells (a
+  // gate/up tile is hidden/inter whole slabs of 8 rows x I); a down slot is 8
+  // cells, one slab per consumer warp.
   const size_t optin = prop.sharedMemPerBlockOptin;
-  const int np_max = kMaxTokens * h->kp();
-  const size_t fixed = layer_smem_bytes(0, np_max, h->ea());
-  const size_t avail = optin > fixed ? optin - fixed : 0;
-  const size_t red = layer_reduction_bytes(fp8);
-  h->s_gu = avail > red ? (int)std::min<size_t>(kMaxGateUpStages, (avail - red) / h->tile_gu) : 0;
-  // The down phase reuses the ring as slab-sized cells (a gate/up tile is
-  // hidden/inter whole slabs of 8 rows x I); a down slot is 8 cells, one
-  // slab per consumer warp.
-  h->ring_bytes = (uint32_t)((size_t)h->s_gu * h->tile_gu + red);
-  h->s_d = (int)std::min<size_t>(kMaxDownStages, h->ring_bytes / ((size_t)kConsumerWarps * h->tile_d));
-  if (h->s_gu < 2 || h->s_d < 2) {
-    set_err("not enough shared memory for the staging rings");
-    free_layer(h);
-    return nullptr;
+  h->n_plans = fp8 ? 2 : 1;
+  for (int i = 0; i < h->n_plans; ++i) {
+    LayerPlan& pl = h->plan[i];
+    const int tb = i == 0 ? 2 : 1;  // token blocks of 8 per group
+    pl.kernel = layer_kernel_for(hidden / 256, variant, fp8, tb);
+    pl.max_tokens = i == 0 ? kMaxTokens : 8;
+    const int np_max = pl.max_tokens * h->kp();
+    const size_t fixed = layer_smem_bytes(0, np_max, h->ea());
+    const size_t avail = optin > fixed ? optin - fixed : 0;
+    const size_t red = layer_reduction_bytes(fp8, tb);
+    pl.s_gu = avail > red ? (int)std::min<size_t>(kMaxGateUpStages, (avail - red) / h->tile_gu) : 0;
+    pl.ring_bytes = (uint32_t)((size_t)pl.s_gu * h->tile_gu + red);
+    pl.s_d = (int)std::min<size_t>(kMaxDownStages, pl.ring_bytes / ((size_t)kConsumerWarps * h->tile_d));
+    if (!pl.kernel || pl.s_gu < 2 || pl.s_d < 2) {
+      set_err("not enough shared memory for the staging rings");
+      free_layer(h);
+      return nullptr;
+    }
+    pl.smem_max = layer_smem_bytes(pl.ring_bytes, np_max, h->ea());
   }
-  h->smem_max = layer_smem_bytes(h->ring_bytes, np_max, h->ea());
 
   AllocCounter ac;
   const size_t E = n_experts, H = hidden, I = inter;
@@ -387,8 +405,12 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   // The expert kernels run one CTA per SM with most of its shared memory;
   // asking for the largest carveout up front avoids a reconfiguration of the
   // L1/shared split between launches.
-  if ((e = cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem_max)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(h->kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100)) != cudaSuccess) {
+  e = cudaSuccess;
+  for (int i = 0; i < h->n_plans && e == cudaSuccess; ++i)
+    if ((e = cudaFuncSetAttribute(h->plan[i].kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)h->plan[i].smem_max)) == cudaSuccess)
+      e = cudaFuncSetAttribute(h->plan[i].kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) {
     cuda_fail(e, "shared-memory attribute");
     free_layer(h);
     return nullptr;
@@ -534,15 +556,15 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
   o->hidden = h->H; o->n_experts = h->E; o->topk = h->K; o->inter = h->I;
   o->max_tokens = MOE_MAX_TOKENS;
   o->n_sms = h->n_sms;
-  o->gateup_stages = h->s_gu;
-  o->down_stages = h->s_d;
+  o->gateup_stages = h->plan[0].s_gu;
+  o->down_stages = h->plan[0].s_d;
   o->gateup_tile_bytes = (int)h->tile_gu;
   o->down_tile_bytes = (int)(h->tile_d * kConsumerWarps);
   o->weight_bytes = h->weight_bytes;
   o->workspace_bytes = h->ws_bytes;
   o->kernels_per_forward = 1;
   o->router_split = h->ks;
-  o->smem_bytes = h->smem_max;
+  o->smem_bytes = h->plan[0].smem_max;
   o->shared_expert = h->shared;
   o->routed_scale = h->routed_scale;
   o->bias_selection_only = h->sel_only;

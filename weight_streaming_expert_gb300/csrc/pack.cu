@@ -22,10 +22,14 @@
 // gate/up (k = H) and ((tile * I/32 + q) * 32 + lane) for down (k = I).
 //
 // E4M3 codes (one byte each): tiles of 16 rows, the same bytes as 8 bf16
-// rows.  A tile is two n8 blocks; lane (g, t)'s 16-byte chunk q holds the
-// codes of block 0's row g at k = 32q + 8t .. +7, then those of block 1's:
-//   gate/up tile (e, tt), block b: n even -> gate row 8tt + 4b + n/2,
-//                                  n odd  -> up row   8tt + 4b + n/2
+// rows, which are the 16 rows of the MMA's A operand (the tokens are B).
+// A tile is two 8-row blocks; lane (g, t)'s 16-byte chunk q holds the codes
+// of block 0's row g at k = 32q + 8t .. +7, then those of block 1's row g --
+// the lane's A registers for rows g and g + 8:
+//   gate/up tile (e, tt): block 0 row n = gate row 8tt + n,
+//                         block 1 row n = up row   8tt + n
+//     (so one lane's accumulators hold the gate and the up value of one
+//     intermediate row: SwiGLU needs no exchange between lanes)
 //   down slab (e, sl), block b: output rows 16sl + 8b .. 16sl + 8b + 7
 #include "kernels.cuh"
 
@@ -85,8 +89,7 @@ __global__ void pack_gate_up_fp8_kernel(const uint2* __restrict__ src, uint4* __
     uint2 v[2];
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
-      const int ri = 8 * tt + 4 * b + (g >> 1);
-      const int row = (g & 1) ? I + ri : ri;
+      const int row = (b ? I : 0) + 8 * tt + g;  // gate rows, then the same up rows
       v[b] = src[((size_t)e * 2 * I + row) * RC + 4 * q + t];
     }
     dst[c] = make_uint4(v[0].x, v[0].y, v[1].x, v[1].y);
