@@ -65,7 +65,8 @@ def source_hash(paths):
 LAYER_SOURCES = [os.path.join(ROOT, "weight_streaming_expert_gb300", "csrc", f)
                  for f in ("layer_kernel.cuh", "routing.cuh", "common.cuh", "kernels.cuh",
                            "layer_kernel_a.cu", "layer_kernel_b.cu", "layer_kernel_c.cu", "layer_kernel_d.cu",
-                           "layer_kernel_e.cu", "layer_kernel_f.cu", "layer_kernel_g.cu", "layer_kernel_h.cu")]
+                           "layer_kernel_e.cu", "layer_kernel_f.cu", "layer_kernel_g.cu", "layer_kernel_h.cu",
+                           "layer_kernel_i.cu", "layer_kernel_j.cu", "layer_kernel_k.cu", "layer_kernel_l.cu")]
 # DRAM traffic records of one ncu capture each: bf16 and fp8 expert weights
 TRAFFIC_FILES = {False: os.path.join(ROOT, "profiles", "layer_traffic.json"),
                  True: os.path.join(ROOT, "profiles", "layer_traffic_fp8.json")}

@@ -236,15 +236,18 @@ typedef struct {
   int max_tokens;          /* MOE_MAX_TOKENS */
   int n_sms;               /* SMs of the device the handle lives on */
   int gateup_stages;       /* shared-memory ring depth of the gate/up phase
-                              (the ring of a call at M = 64: an fp8 layer's
-                              calls with M <= 8 run a second instance with a
+                              (the ring of a call at M = 64: calls with
+                              M <= 8 run a second instance, with one token
+                              set per expert group; an fp8 layer's has a
                               smaller reduction area and deeper rings) */
   int down_stages;         /* shared-memory stages of the down phase (M = 64) */
   int gateup_tile_bytes;   /* bytes of one gate/up weight tile (8 bf16 or
                               16 fp8 rows x H) */
-  int down_tile_bytes;     /* bytes of one down super tile (8 slabs of
-                              8 bf16 or 16 fp8 rows x I, one per consumer
-                              warp) */
+  int down_tile_bytes;     /* bytes of one down super tile at M = 64: 8
+                              cells, one per consumer warp, of one slab (8
+                              bf16 or 16 fp8 rows x I) each; a bf16 layer's
+                              calls with M <= 8 use cells of up to 512 / I
+                              slabs (64 KB super tiles) */
   size_t weight_bytes;     /* device bytes held for the weights */
   size_t workspace_bytes;  /* device bytes held for the workspace */
   int kernels_per_forward; /* kernel launches per forward call (1) */

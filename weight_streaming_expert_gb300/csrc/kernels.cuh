@@ -23,9 +23,10 @@ struct LayerArgs {
   int M, H, E, K, I;
   int ks;                         // hidden-dim split of the router matvec
   int gu_stages;                  // gate/up ring depth
-  int d_stages;                   // down slots of one super tile (8 slabs) each
+  int d_stages;                   // down slots of one super tile (8 cells) each
   uint32_t gu_tile;               // 8 rows x H x 2 bytes
-  uint32_t d_tile;                // 8 rows x I x 2 bytes
+  uint32_t d_tile;                // one down cell: d_spw slabs of 8 rows x I x 2 bytes
+  int d_spw;                      // down slabs per cell (a consumer warp's unit; <= 512 / I)
   uint32_t ring_bytes;            // gu_stages*gu_tile + the reduction area
   int trace;                      // record phase timestamps
   int shared;                     // 1: expert E is a shared expert every token passes (weight 1)
@@ -38,7 +39,7 @@ struct LayerArgs {
 // layer_smem_bytes(ring_bytes, NP, buckets).  KPW = H/256.
 using LayerKernel = void (*)(LayerArgs);
 // variant: the instance that handles the layer variants; fp8: the instance
-// for E4M3 expert weights (plain layers only) whose groups hold up to
+// for E4M3 expert weights (plain layers only); token_blocks: groups of up to
 // 8 x token_blocks tokens (1: calls with M <= 8; 2: any call).  nullptr: no
 // such instance.
 LayerKernel layer_kernel_for(int kpw, bool variant, bool fp8 = false, int token_blocks = 2);

@@ -98,6 +98,10 @@ static_assert(kOffCall + 8 <= kOffTile && kOffTile + 4 * kMaxGateUpStages <= kOf
 static_assert(kRingOff % 128 == 0, "ring alignment");
 static_assert(kMaxGateUpStages < kRedSlots, "reduction slots must outnumber ring stages");
 
+struct OneSlab {  // a down cell of one slab, as a compile-time count
+  __device__ constexpr operator int() const { return 1; }
+};
+
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Count this CTA in at a grid-wide counter: release fence, then an atomic
@@ -172,13 +176,16 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g));
 // FP8: expert weights as E4M3 codes with fp32 per-row scales -- tiles of 16
 // rows (the same bytes as 8 bf16 rows), codes converted to f16 in registers,
 // tokens and h converted to f16 per group, the row scales applied in fp32
-// after the sums (reducer and down epilogue).  TB = 1 serves groups of at
-// most 8 tokens (calls with M <= 8): the weights are the MMA's A operand
-// (its 16 rows are the tile's two 8-row blocks) and the tokens one n8 B
-// block -- two MMAs per 16-byte chunk and one set of token registers.
-// TB = 2 serves groups of up to 16: the 16 tokens are A and each 8-row
-// block of the tile a B operand (four MMAs per chunk).  bf16 weights: tokens
-// are A, the 8-row tile B; TB is unused.
+// after the sums (reducer and down epilogue).
+// TB: token blocks of 8 per group.  TB = 2 serves groups of up to 16 tokens
+// (any call): the group's tokens are the MMA's A operand (16 rows) and the
+// weights B (bf16: the 8-row tile; fp8: each of the tile's two 8-row blocks,
+// four MMAs per 16-byte chunk).  TB = 1 serves groups of at most 8 tokens
+// (calls with M <= 8) and holds one set of token registers instead of two
+// (the two sets are 40 to 128 registers of a 168-register budget): bf16 still
+// puts the tokens in A, the same 8 rows in both halves (rows 8..15 of C are
+// never stored); fp8 swaps the operands -- the tile's 16 weight rows are A
+// and the tokens one n8 B block, two MMAs per chunk.
 template <int KPW, bool VARIANT, bool FP8, int TB>
 __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs a) {
   using namespace layer_detail;
@@ -190,8 +197,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   constexpr int D_ROWS = FP8 ? 16 : kDownTileRows;     // output rows per down slab
   static_assert(TB == 1 || TB == 2, "token blocks");
   constexpr bool WA = FP8 && TB == 1;                  // the weights are the MMA's A operand
+  constexpr bool TWO = TB == 2;                        // a second token set (group rows 8..15)
   constexpr int NB = FP8 && TB == 2 ? 2 : 1;           // float4 partials per lane (gate/up reduction)
-  const int NSL = kConsumerWarps, SD = a.d_stages;  // slabs per down super tile, down slots
+  const int NSL = kConsumerWarps, SD = a.d_stages;  // cells per down super tile, down slots
+  const int SPW = a.d_spw;                           // down slabs per cell
   const int MK = a.M * a.K;                     // routed pairs (token * K + slot)
   const bool shared = VARIANT && a.shared;
   const int NP = MK + (shared ? a.M : 0);       // + the shared expert's pairs MK + token
@@ -328,13 +337,13 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
 
   const int TPG = 2 * a.I / GU_ROWS;          // gate/up tiles per group
   const int T_gu = n_groups * TPG;
-  const int SL = a.H / D_ROWS;                // output slabs per group (the down GEMV's unit)
-  const int SPG = SL / NSL;                   // down super tiles per group
+  const int CL = a.H / (D_ROWS * SPW);        // down cells per group (SPW output slabs each)
+  const int SPG = CL / NSL;                   // down super tiles per group
   const int T_d = n_groups * SPG;
   // groups [0, g_static) are split statically in both GEMVs: their gate/up
   // tiles are all in the static share, and so are their down tiles
   const int g_static = n_groups * kStaticNum / kStaticDen;
-  // The down phase reuses the ring as cells of one slab (d_tile bytes; a
+  // The down phase reuses the ring as cells of SPW slabs (d_tile bytes; a
   // gate/up stage is exactly cps cells, the reduction area behind the
   // stages holds the rest).  Gate/up stage (n_gu + r) mod S is released for
   // the last time r-th (n_gu = this CTA's gate/up tile count; stages it
@@ -514,7 +523,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       {  // the 8 slabs are contiguous in global memory; one copy per run of
          // adjacent cells, the runs worked out arithmetically (list positions
          // 8s .. 8s + 7, stage boundaries every cps positions)
-        const uint8_t* src = a.w_down + ((size_t)cur_de * SL + (size_t)q * NSL) * a.d_tile;
+        const uint8_t* src = a.w_down + ((size_t)cur_de * CL + (size_t)q * NSL) * a.d_tile;
         int p = s * kConsumerWarps, left = NSL, w0 = 0;
         int r = p / cps, within = p - r * cps;
         while (left > 0) {
@@ -562,7 +571,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   {
     // ---- 4. gate/up + SwiGLU
     uint4 xa[KPW], xb[KPW];  // token rows g4 and g4 + 8 of the group: this warp's k chunks
-                             // (weights as A: row g4 only)
+                             // (TB = 1: row g4 only)
     int cur_g = -1, start = 0, cnt = 0;
     // this CTA's statically split tiles come first: after the last of them
     // (or at once if it has none) the warp reports them reduced
@@ -593,10 +602,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
 #pragma unroll
         for (int q = 0; q < KPW; ++q) {
           xa[q] = x0[4 * (warp * KPW + q)];
-          if constexpr (!WA) xb[q] = x1[4 * (warp * KPW + q)];
+          if constexpr (TWO) xb[q] = x1[4 * (warp * KPW + q)];
           if constexpr (FP8) {
             xa[q] = bf16x8_to_f16x8(xa[q]);
-            if constexpr (!WA) xb[q] = bf16x8_to_f16x8(xb[q]);
+            if constexpr (TWO) xb[q] = bf16x8_to_f16x8(xb[q]);
           }
         }
         cur_g = g;
@@ -649,8 +658,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
           mma_f16(c1, xa[q].x, xb[q].x, xa[q].y, xb[q].y, f0, f1);
           mma_f16(c1, xa[q].z, xb[q].z, xa[q].w, xb[q].w, f2, f3);
         } else {
-          mma_bf16(c0, xa[q].x, xb[q].x, xa[q].y, xb[q].y, b.x, b.y);
-          mma_bf16(c1, xa[q].z, xb[q].z, xa[q].w, xb[q].w, b.z, b.w);
+          const uint4 xh = TWO ? xb[q] : xa[q];  // A rows 8..15
+          mma_bf16(c0, xa[q].x, xh.x, xa[q].y, xh.y, b.x, b.y);
+          mma_bf16(c1, xa[q].z, xh.z, xa[q].w, xh.w, b.z, b.w);
         }
       }
       __syncwarp();
@@ -729,9 +739,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
 
   {
     // ---- 5. down GEMV, weighted rows y[pair] = w_pair * (W_d h_pair);
-    // warp w takes slab w of every super tile
+    // warp w takes cell w of every super tile: SPW consecutive output slabs
     const int kpd = a.I / 32;  // 32-wide k chunks of a down row (<= kMaxDownChunks)
-    uint4 ha[kMaxDownChunks], hb[kMaxDownChunks];  // h rows of group tokens g4, g4 + 8 (weights as A: g4)
+    uint4 ha[kMaxDownChunks], hb[kMaxDownChunks];  // h rows of group tokens g4, g4 + 8 (TB = 1: g4)
     // the pairs this lane stores: weights as A, group tokens 2 t4 and
     // 2 t4 + 1; otherwise tokens g4 and g4 + 8
     int pid[2] = {-1, -1};
@@ -747,7 +757,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       const int tile = dstage_tile[s];
       if (tile < 0) break;
       const int g = tile / SPG;
-      const int sl = (tile - g * SPG) * NSL + warp;
+      const int cl = (tile - g * SPG) * NSL + warp;  // this warp's cell: slabs cl SPW .. cl SPW + SPW - 1
       if (g != cur_g) {
         const int start = rt.grp_start[g], cnt = rt.grp_cnt[g];
         const uint4* h0 =
@@ -758,10 +768,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         for (int q = 0; q < kMaxDownChunks; ++q) {
           if (q < kpd) {
             ha[q] = __ldcg(h0 + 4 * q);  // written by other SMs in this grid: L2, not L1
-            if constexpr (!WA) hb[q] = __ldcg(h1 + 4 * q);
+            if constexpr (TWO) hb[q] = __ldcg(h1 + 4 * q);
             if constexpr (FP8) {
               ha[q] = bf16x8_to_f16x8(ha[q]);
-              if constexpr (!WA) hb[q] = bf16x8_to_f16x8(hb[q]);
+              if constexpr (TWO) hb[q] = bf16x8_to_f16x8(hb[q]);
             }
           }
         }
@@ -774,94 +784,120 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         }
         cur_g = g;
       }
-      // fp8 scales of the output rows, loaded while the data lands: weights
-      // as A, rows 16 sl + g4 and + 8 in (rs.x, rs.y); as B, rows
-      // 16 sl + 8 b + 2 t4 and + 1 of block b in (rs.x, rs.y) and (rs.z, rs.w)
-      float4 rs = make_float4(1.f, 1.f, 1.f, 1.f);
-      if constexpr (WA) {
-        const float* sd = a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + g4;
-        rs.x = __ldg(sd);
-        rs.y = __ldg(sd + 8);
-      } else if constexpr (FP8) {
-        const float* sd = a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + 2 * t4;
-        const float2 r0 = __ldg(reinterpret_cast<const float2*>(sd));
-        const float2 r1 = __ldg(reinterpret_cast<const float2*>(sd + 8));
-        rs = make_float4(r0.x, r0.y, r1.x, r1.y);
-      }
-      if (!warp_wait(dfull(s), ph, &waited)) {
-        record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dfull(s), waited);
-        break;
-      }
-      if (j == 0 && tid == 0) stamp(a, 14);
-      // bf16 and fp8 with weights as A: c0, c1 = the two k-steps; fp8 with
-      // weights as B: c0, c1 = the slab's two 8-row blocks
-      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint4* bp =
-          reinterpret_cast<const uint4*>(ring + (size_t)cell_tab[s * kConsumerWarps + warp] * a.d_tile) + lane;
-#pragma unroll
-      for (int q = 0; q < kMaxDownChunks; ++q) {
-        if (q < kpd) {
-          const uint4 b = bp[q * 32];
-          if constexpr (WA) {  // b.x, b.y: output row 16 sl + g4; b.z, b.w: row 16 sl + 8 + g4
-            uint32_t p0, p1, p2, p3, r0, r1, r2, r3;
-            e4m3x4_to_f16x2(b.x, p0, p1);
-            e4m3x4_to_f16x2(b.y, p2, p3);
-            e4m3x4_to_f16x2(b.z, r0, r1);
-            e4m3x4_to_f16x2(b.w, r2, r3);
-            mma_f16(c0, p0, r0, p1, r1, ha[q].x, ha[q].y);
-            mma_f16(c1, p2, r2, p3, r3, ha[q].z, ha[q].w);
-          } else if constexpr (FP8) {  // the same codes, as the B columns of the two blocks
-            uint32_t f0, f1, f2, f3;
-            e4m3x4_to_f16x2(b.x, f0, f1);
-            e4m3x4_to_f16x2(b.y, f2, f3);
-            mma_f16(c0, ha[q].x, hb[q].x, ha[q].y, hb[q].y, f0, f1);
-            mma_f16(c0, ha[q].z, hb[q].z, ha[q].w, hb[q].w, f2, f3);
-            e4m3x4_to_f16x2(b.z, f0, f1);
-            e4m3x4_to_f16x2(b.w, f2, f3);
-            mma_f16(c1, ha[q].x, hb[q].x, ha[q].y, hb[q].y, f0, f1);
-            mma_f16(c1, ha[q].z, hb[q].z, ha[q].w, hb[q].w, f2, f3);
+      // fp8 scales of slab sl's output rows: weights as A, rows 16 sl + g4 and
+      // + 8 in (rs.x, rs.y); as B, rows 16 sl + 8 b + 2 t4 and + 1 of block b
+      // in (rs.x, rs.y) and (rs.z, rs.w)
+      auto row_scales = [&](int sl) -> float4 {
+        float4 r = make_float4(1.f, 1.f, 1.f, 1.f);
+        if constexpr (WA) {
+          const float* sd = a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + g4;
+          r.x = __ldg(sd);
+          r.y = __ldg(sd + 8);
+        } else if constexpr (FP8) {
+          const float* sd = a.s_d + (size_t)cur_de * a.H + sl * D_ROWS + 2 * t4;
+          const float2 r0 = __ldg(reinterpret_cast<const float2*>(sd));
+          const float2 r1 = __ldg(reinterpret_cast<const float2*>(sd + 8));
+          r = make_float4(r0.x, r0.y, r1.x, r1.y);
+        }
+        return r;
+      };
+      // The cell's NS slabs.  A compile-time 1 (no loop) in every instance but
+      // bf16 with TB = 1, whose cells hold SPW slabs (run-time: more than one
+      // where I < 512).  A looping copy of this body costs the other
+      // instances registers (spills at TB = 2) or, in the fp8 consumers,
+      // which are bound by their own instructions, measurable time.
+      auto consume_cell = [&](auto ns) -> bool {
+        const int NS = ns;
+        float4 rs = row_scales(cl * NS);  // the first slab's, while the data lands
+        if (!warp_wait(dfull(s), ph, &waited)) {
+          record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dfull(s), waited);
+          return false;
+        }
+        if (j == 0 && tid == 0) stamp(a, 14);
+        const uint4* bp =
+            reinterpret_cast<const uint4*>(ring + (size_t)cell_tab[s * kConsumerWarps + warp] * a.d_tile) + lane;
+        for (int u = 0; u < NS; ++u) {
+          const int sl = cl * NS + u;
+          if (u > 0) rs = row_scales(sl);
+          // bf16 and fp8 with weights as A: c0, c1 = the two k-steps; fp8 with
+          // weights as B: c0, c1 = the slab's two 8-row blocks
+          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+          for (int q = 0; q < kMaxDownChunks; ++q) {
+            if (q < kpd) {
+              const uint4 b = bp[(u * kpd + q) * 32];
+              if constexpr (WA) {  // b.x, b.y: output row 16 sl + g4; b.z, b.w: row 16 sl + 8 + g4
+                uint32_t p0, p1, p2, p3, r0, r1, r2, r3;
+                e4m3x4_to_f16x2(b.x, p0, p1);
+                e4m3x4_to_f16x2(b.y, p2, p3);
+                e4m3x4_to_f16x2(b.z, r0, r1);
+                e4m3x4_to_f16x2(b.w, r2, r3);
+                mma_f16(c0, p0, r0, p1, r1, ha[q].x, ha[q].y);
+                mma_f16(c1, p2, r2, p3, r3, ha[q].z, ha[q].w);
+              } else if constexpr (FP8) {  // the same codes, as the B columns of the two blocks
+                uint32_t f0, f1, f2, f3;
+                e4m3x4_to_f16x2(b.x, f0, f1);
+                e4m3x4_to_f16x2(b.y, f2, f3);
+                mma_f16(c0, ha[q].x, hb[q].x, ha[q].y, hb[q].y, f0, f1);
+                mma_f16(c0, ha[q].z, hb[q].z, ha[q].w, hb[q].w, f2, f3);
+                e4m3x4_to_f16x2(b.z, f0, f1);
+                e4m3x4_to_f16x2(b.w, f2, f3);
+                mma_f16(c1, ha[q].x, hb[q].x, ha[q].y, hb[q].y, f0, f1);
+                mma_f16(c1, ha[q].z, hb[q].z, ha[q].w, hb[q].w, f2, f3);
+              } else {
+                const uint4 hh = TWO ? hb[q] : ha[q];  // A rows 8..15
+                mma_bf16(c0, ha[q].x, hh.x, ha[q].y, hh.y, b.x, b.y);
+                mma_bf16(c1, ha[q].z, hh.z, ha[q].w, hh.w, b.z, b.w);
+              }
+            }
+          }
+          if (u == NS - 1) {
+            __syncwarp();  // every lane has read the whole cell
+            if (lane == 0) mbar_arrive(dempty(s));
+          }
+          if constexpr (WA) {
+            // c0 + c1: (rows 16 sl + g4 | 16 sl + 8 + g4) x (tokens 2 t4, 2 t4 + 1)
+            const int row = sl * D_ROWS + g4;
+  #pragma unroll
+            for (int i = 0; i < 2; ++i)
+              if (pid[i] >= 0) {
+                float* yr = a.ws.y + (size_t)pid[i] * a.H + row;
+                yr[0] = pw[i] * (rs.x * (c0[i] + c1[i]));
+                yr[8] = pw[i] * (rs.y * (c0[2 + i] + c1[2 + i]));
+              }
+          } else if constexpr (FP8) {
+            // block b: (token g4 | g4 + 8) x (rows 16 sl + 8 b + 2 t4, + 1)
+            const int row = sl * D_ROWS + 2 * t4;
+  #pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              const float* v = b ? c1 : c0;
+              const float sx = b ? rs.z : rs.x, sy = b ? rs.w : rs.y;
+              if (pid[0] >= 0)
+                *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row + 8 * b) =
+                    make_float2(pw[0] * (sx * v[0]), pw[0] * (sy * v[1]));
+              if (pid[1] >= 0)
+                *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row + 8 * b) =
+                    make_float2(pw[1] * (sx * v[2]), pw[1] * (sy * v[3]));
+            }
           } else {
-            mma_bf16(c0, ha[q].x, hb[q].x, ha[q].y, hb[q].y, b.x, b.y);
-            mma_bf16(c1, ha[q].z, hb[q].z, ha[q].w, hb[q].w, b.z, b.w);
+            // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of the slab)
+            const int row = sl * D_ROWS + 2 * t4;
+            if (pid[0] >= 0)
+              *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row) =
+                  make_float2(pw[0] * (c0[0] + c1[0]), pw[0] * (c0[1] + c1[1]));
+            if (pid[1] >= 0)
+              *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row) =
+                  make_float2(pw[1] * (c0[2] + c1[2]), pw[1] * (c0[3] + c1[3]));
           }
         }
-      }
-      __syncwarp();  // every lane has read the stage
-      if (lane == 0) mbar_arrive(dempty(s));
-      if constexpr (WA) {
-        // c0 + c1: (rows 16 sl + g4 | 16 sl + 8 + g4) x (tokens 2 t4, 2 t4 + 1)
-        const int row = sl * D_ROWS + g4;
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (pid[i] >= 0) {
-            float* yr = a.ws.y + (size_t)pid[i] * a.H + row;
-            yr[0] = pw[i] * (rs.x * (c0[i] + c1[i]));
-            yr[8] = pw[i] * (rs.y * (c0[2 + i] + c1[2 + i]));
-          }
-      } else if constexpr (FP8) {
-        // block b: (token g4 | g4 + 8) x (rows 16 sl + 8 b + 2 t4, + 1)
-        const int row = sl * D_ROWS + 2 * t4;
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const float* v = b ? c1 : c0;
-          const float sx = b ? rs.z : rs.x, sy = b ? rs.w : rs.y;
-          if (pid[0] >= 0)
-            *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row + 8 * b) =
-                make_float2(pw[0] * (sx * v[0]), pw[0] * (sy * v[1]));
-          if (pid[1] >= 0)
-            *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row + 8 * b) =
-                make_float2(pw[1] * (sx * v[2]), pw[1] * (sy * v[3]));
-        }
-      } else {
-        // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of the slab)
-        const int row = sl * D_ROWS + 2 * t4;
-        if (pid[0] >= 0)
-          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row) =
-              make_float2(pw[0] * (c0[0] + c1[0]), pw[0] * (c0[1] + c1[1]));
-        if (pid[1] >= 0)
-          *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row) =
-              make_float2(pw[1] * (c0[2] + c1[2]), pw[1] * (c0[3] + c1[3]));
-      }
+        return true;
+      };
+      bool cell_ok;
+      if constexpr (FP8 || TWO)
+        cell_ok = consume_cell(OneSlab{});
+      else
+        cell_ok = consume_cell(SPW);
+      if (!cell_ok) break;
     }
     if (tid == 0) stamp(a, 7);
   }

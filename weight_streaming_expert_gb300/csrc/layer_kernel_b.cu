@@ -1,5 +1,5 @@
 // layer_kernel_b.cu -- layer kernel instances for hidden = 256 x {8,10,12,16}, plain
-// (one of eight translation units compiled in parallel).
+// (one of twelve translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {
@@ -21,6 +21,10 @@ LayerKernel layer_kernel_fp8_small(int kpw);
 LayerKernel layer_kernel_fp8_large(int kpw);
 LayerKernel layer_kernel_fp8_small_tb1(int kpw);
 LayerKernel layer_kernel_fp8_large_tb1(int kpw);
+LayerKernel layer_kernel_plain_small_tb1(int kpw);
+LayerKernel layer_kernel_plain_large_tb1(int kpw);
+LayerKernel layer_kernel_variant_small_tb1(int kpw);
+LayerKernel layer_kernel_variant_large_tb1(int kpw);
 
 LayerKernel layer_kernel_for(int kpw, bool variant, bool fp8, int token_blocks) {
   if (fp8) {
@@ -33,8 +37,16 @@ LayerKernel layer_kernel_for(int kpw, bool variant, bool fp8, int token_blocks) 
     return k ? k : layer_kernel_fp8_small(kpw);
   }
   if (variant) {
+    if (token_blocks == 1) {
+      const LayerKernel k = layer_kernel_variant_large_tb1(kpw);
+      return k ? k : layer_kernel_variant_small_tb1(kpw);
+    }
     const LayerKernel k = layer_kernel_variant_large(kpw);
     return k ? k : layer_kernel_variant_small(kpw);
+  }
+  if (token_blocks == 1) {
+    const LayerKernel k = layer_kernel_plain_large_tb1(kpw);
+    return k ? k : layer_kernel_plain_small_tb1(kpw);
   }
   const LayerKernel k = layer_kernel_plain_large(kpw);
   return k ? k : layer_kernel_plain_small(kpw);

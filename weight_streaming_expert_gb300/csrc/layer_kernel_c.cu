@@ -1,5 +1,5 @@
 // layer_kernel_c.cu -- layer kernel instances for hidden = 256 x {1,2,4,5}, layer variants
-// (one of eight translation units compiled in parallel).
+// (one of twelve translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {

@@ -1,5 +1,5 @@
 // layer_kernel_d.cu -- layer kernel instances for hidden = 256 x {8,10,12,16}, layer variants
-// (one of eight translation units compiled in parallel).
+// (one of twelve translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {

@@ -1,5 +1,5 @@
 // layer_kernel_e.cu -- layer kernel instances for hidden = 256 x {1,2,4,5}, fp8 expert weights,
-// groups of up to 16 tokens (one of eight translation units compiled in parallel).
+// groups of up to 16 tokens (one of twelve translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {

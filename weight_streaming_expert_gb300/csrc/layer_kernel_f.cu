@@ -1,5 +1,5 @@
 // layer_kernel_f.cu -- layer kernel instances for hidden = 256 x {8,10,12,16}, fp8 expert weights,
-// groups of up to 16 tokens (one of eight translation units compiled in parallel).
+// groups of up to 16 tokens (one of twelve translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {

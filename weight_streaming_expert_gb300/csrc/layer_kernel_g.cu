@@ -1,5 +1,5 @@
 // layer_kernel_g.cu -- layer kernel instances for hidden = 256 x {1,2,4,5}, fp8 expert weights,
-// groups of at most 8 tokens (calls with M <= 8) (one of eight translation units compiled in parallel).
+// groups of at most 8 tokens (calls with M <= 8) (one of twelve translation units compiled in parallel).
 #include "layer_kernel.cuh"
 
 namespace wse {

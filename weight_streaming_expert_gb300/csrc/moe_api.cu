@@ -68,6 +68,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct LayerPlan {
   LayerKernel kernel = nullptr;
   int max_tokens = 0;
+  int d_spw = 1;            // down slabs per cell
+  uint32_t tile_d = 0;      // down cell bytes
   int s_gu = 0, s_d = 0;    // gate/up ring depth, down stages
   uint32_t ring_bytes = 0;
   size_t smem_max = 0;      // dynamic shared memory at M = max_tokens
@@ -94,12 +96,12 @@ struct moe_layer {
   size_t ws_bytes = 0, weight_bytes = 0;
   Workspace ws{};
   int ks = 1;               // hidden-dim split of the router matvec
-  uint32_t tile_gu = 0, tile_d = 0;
-  // plan[0] serves every M; an fp8 layer's plan[1] serves M <= 8 (groups of
-  // at most 8 tokens: one token block, half the reduction area)
+  uint32_t tile_gu = 0;     // gate/up tile bytes
+  // plan[0] serves every M, plan[1] calls with M <= 8 (groups of at most 8
+  // tokens: one token block -- half the token registers; fp8: half the
+  // MMAs and half the reduction area)
   LayerPlan plan[2];
-  int n_plans = 1;
-  const LayerPlan& plan_for(int M) const { return n_plans > 1 && M <= plan[1].max_tokens ? plan[1] : plan[0]; }
+  const LayerPlan& plan_for(int M) const { return M <= plan[1].max_tokens ? plan[1] : plan[0]; }
   std::map<int, GraphEntry> graphs;
   cudaStream_t cap_stream = nullptr;
 };
@@ -154,7 +156,8 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   la.gu_stages = pl.s_gu;
   la.d_stages = pl.s_d;
   la.gu_tile = h->tile_gu;
-  la.d_tile = h->tile_d;
+  la.d_tile = pl.tile_d;
+  la.d_spw = pl.d_spw;
   la.ring_bytes = pl.ring_bytes;
   la.trace = trace ? 1 : 0;
   la.shared = h->shared;
@@ -284,7 +287,6 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   h->dev = dev;
   h->n_sms = prop.multiProcessorCount;
   h->tile_gu = (uint32_t)(kGateUpTileRows * hidden * 2);
-  h->tile_d = (uint32_t)(kDownTileRows * inter * 2);
   h->ks = gemv_split(hidden, n_experts, h->n_sms);
 
   // Rings sized for the largest call of each plan: the gate/up stages plus
@@ -295,19 +297,34 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   // gate/up tile is hidden/inter whole slabs of 8 rows x I); a down slot is 8
   // cells, one slab per consumer warp.
   const size_t optin = prop.sharedMemPerBlockOptin;
-  h->n_plans = fp8 ? 2 : 1;
-  for (int i = 0; i < h->n_plans; ++i) {
+  for (int i = 0; i < 2; ++i) {
     LayerPlan& pl = h->plan[i];
     const int tb = i == 0 ? 2 : 1;  // token blocks of 8 per group
     pl.kernel = layer_kernel_for(hidden / 256, variant, fp8, tb);
     pl.max_tokens = i == 0 ? kMaxTokens : 8;
+    // A down cell (one consumer warp's unit of a super tile) is d_spw
+    // consecutive output slabs.  The bf16 instances for M <= 8 take as many
+    // as keep it within 8 rows x 512 bf16 (8 KB, whatever inter is: small
+    // cells make every copy's fixed cost dominate) while super tiles (8
+    // cells) and gate/up stages stay whole; the others take one.
+    if (!fp8 && tb == 1)
+      while (2 * pl.d_spw * inter <= 512 && hidden % (kDownTileRows * kConsumerWarps * 2 * pl.d_spw) == 0 &&
+             hidden % (inter * 2 * pl.d_spw) == 0)
+        pl.d_spw *= 2;
+    pl.tile_d = (uint32_t)(kDownTileRows * inter * 2 * pl.d_spw);
     const int np_max = pl.max_tokens * h->kp();
     const size_t fixed = layer_smem_bytes(0, np_max, h->ea());
     const size_t avail = optin > fixed ? optin - fixed : 0;
     const size_t red = layer_reduction_bytes(fp8, tb);
     pl.s_gu = avail > red ? (int)std::min<size_t>(kMaxGateUpStages, (avail - red) / h->tile_gu) : 0;
-    pl.ring_bytes = (uint32_t)((size_t)pl.s_gu * h->tile_gu + red);
-    pl.s_d = (int)std::min<size_t>(kMaxDownStages, pl.ring_bytes / ((size_t)kConsumerWarps * h->tile_d));
+    // Small gate/up tiles (small hidden) can leave the ring short of two
+    // down super tiles: it then grows to two where the shared memory allows
+    // (cells past the reduction area are down-only, free once the gate/up
+    // loop is done, like the reduction area's).
+    const size_t dsuper = (size_t)kConsumerWarps * pl.tile_d;
+    const size_t ring_gu = (size_t)pl.s_gu * h->tile_gu + red;
+    pl.ring_bytes = (uint32_t)(ring_gu < 2 * dsuper && 2 * dsuper <= avail ? 2 * dsuper : ring_gu);
+    pl.s_d = (int)std::min<size_t>(kMaxDownStages, pl.ring_bytes / dsuper);
     if (!pl.kernel || pl.s_gu < 2 || pl.s_d < 2) {
       set_err("not enough shared memory for the staging rings");
       free_layer(h);
@@ -406,7 +423,7 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   // asking for the largest carveout up front avoids a reconfiguration of the
   // L1/shared split between launches.
   e = cudaSuccess;
-  for (int i = 0; i < h->n_plans && e == cudaSuccess; ++i)
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i)
     if ((e = cudaFuncSetAttribute(h->plan[i].kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)h->plan[i].smem_max)) == cudaSuccess)
       e = cudaFuncSetAttribute(h->plan[i].kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -559,7 +576,7 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
   o->gateup_stages = h->plan[0].s_gu;
   o->down_stages = h->plan[0].s_d;
   o->gateup_tile_bytes = (int)h->tile_gu;
-  o->down_tile_bytes = (int)(h->tile_d * kConsumerWarps);
+  o->down_tile_bytes = (int)(h->plan[0].tile_d * kConsumerWarps);
   o->weight_bytes = h->weight_bytes;
   o->workspace_bytes = h->ws_bytes;
   o->kernels_per_forward = 1;
