@@ -317,7 +317,7 @@ def time_kernel_alone(wkl, calls):
     return np.array([ev[0].elapsed_time(ev[1]) for ev in evs])
 
 
-# trace slots (moe_read_trace): 0 wait passed, 1 matvec done, 2 grid barrier,
+# trace slots (moe_read_trace): 0 wait passed, 1 matvec done, 12 top-k done,
 # 3 routing ready, 4 first gate/up tile, 5 gate/up left, 6 h rows of all CTAs,
 # 7 down left, 8 combine done, 9 last gate/up issue, 10 down prefetch issued
 def phase_breakdown(wkl, reps=2):
@@ -343,7 +343,7 @@ def phase_breakdown(wkl, reps=2):
         t0 = t[:, 0].min()
         r = (t - t0) / 1000.0
         rows.append({
-            "matvec_done": r[:, 1].max(), "grid_barrier": r[:, 2].max(), "routing_ready": r[:, 3].max(),
+            "matvec_done": r[:, 1].max(), "topk_done": r[:, 12].max(), "routing_ready": r[:, 3].max(),
             "first_gateup_tile_median": float(np.median(r[:, 4])), "gateup_end_min": r[:, 5].min(),
             "gateup_end_max": r[:, 5].max(), "h_ready": r[:, 6].max(), "down_end_min": r[:, 7].min(),
             "down_end_max": r[:, 7].max(), "combine_end": r[:, 8].max(),

@@ -5,7 +5,7 @@
  *   router gate matvec -> softmax top-k with renormalisation -> on-device
  *   token->expert compaction -> fused gate/up GEMV + SwiGLU -> down GEMV with
  *   the routing-weighted combine in its epilogue.
- * One persistent kernel (one CTA per SM, grid-wide barriers inside), chained
+ * One persistent kernel (one CTA per SM, grid-wide waits inside), chained
  * to the previous work on the stream with Programmatic Dependent Launch and
  * capturable in a CUDA graph.  No host synchronisation, no allocation and no
  * device->host copy happens inside the forward call.  The kernel needs the
@@ -285,7 +285,7 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
  * MOE_FWD_TRACE (synchronises the device; profiling aid).
  *   out   host uint64 [cap]: for CTA c, slots [32c, 32c + 32) hold
  *         %globaltimer values in ns: 0 dependency wait passed, 1 router
- *         matvec done, 2 grid barrier passed, 3 top-k + compaction done,
+ *         matvec done, 2 (unused), 3 top-k + compaction done,
  *         4 first gate/up tile consumed, 5 gate/up loop left, 6 every CTA's
  *         statically split gate/up tiles reduced (publisher), 7 down loop
  *         left, 8 combine done (the CTAs that combine), 9 producer issued

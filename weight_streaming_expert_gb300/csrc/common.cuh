@@ -29,15 +29,21 @@ constexpr int kTraceSlots = 32;       // per-CTA phase timestamps of a traced ca
 
 // Grid-wide synchronisation words (unsigned, 128 bytes apart).  The 64-bit
 // counts are never reset: each call adds exactly one arrival per CTA to each
-// of the last two and two (the two barriers) to the first, so the barrier
-// after the router tells every CTA the call's index and every later target.
+// of them.  A call starts only once the previous call on the same workspace
+// has completed (stream order, or the PDL dependency wait), so every CTA
+// reads the same kSyncCount at its start: count / grid = calls completed,
+// which gives the call's index (1, 2, ...) and every later target.  The two
+// work counters come in two sets used by odd and even calls; each call
+// clears the other set for the next one.
 enum : int {
-  kSyncCount = 0,         // 64-bit: arrivals at the grid barriers (after the router, before the combine)
-  kSyncGateUpNext = 32,   // next gate/up tile of the dynamically shared tail
-  kSyncDownNext = 64,     // next down super tile of the dynamically shared tail
+  kSyncCount = 0,         // 64-bit: arrivals before the combine (one per CTA per call)
+  kSyncGateUpNext = 32,   // next gate/up tile of the dynamically shared tail (even calls)
+  kSyncDownNext = 64,     // next down super tile of the dynamically shared tail (even calls)
   kSyncStaticDone = 96,   // 64-bit: CTAs whose statically assigned gate/up tiles are reduced
   kSyncGateUpDone = 128,  // 64-bit: CTAs whose gate/up tiles are all reduced
-  kSyncWords = 160,
+  kSyncGateUpNextOdd = 160,
+  kSyncDownNextOdd = 192,
+  kSyncWords = 224,
 };
 
 // A bounded wait gives up after this long (the kernels run for microseconds;
@@ -58,7 +64,7 @@ struct Workspace {
   int* status;               // [1] sticky error bits
   unsigned long long* diag;  // [4] first timeout: where, elapsed ns, raw barrier word, thread/grid
   unsigned* sync;            // [kSyncWords] grid-wide counters, see above
-  float* part;               // [ks][kMaxTokens][E] partial router logits
+  float* part;               // [2][ks][kMaxTokens][E] partial router logits (odd / even calls)
   int* n_groups;             // [1] copy of the call's compaction (inspection only)
   int* n_active;             // [1]
   int* grp_expert;           // [kMaxPairs]

@@ -1,5 +1,5 @@
 // layer_kernel.cuh -- one routed-MoE layer call as ONE persistent kernel:
-// router matvec -> grid barrier -> softmax top-k + compaction -> gate/up
+// router matvec -> tagged partial logits -> softmax top-k + compaction -> gate/up
 // GEMV with SwiGLU -> down GEMV with the weighted combine.
 //
 // Method (page "How Ling-3.0-flash reduces batch 1 decoding latency by 54%
@@ -24,11 +24,15 @@
 // no fence or atomic round trip ever stalls a thread that streams).
 //  1. Prologue, before the dependency wait: barriers, the CTA's slice of
 //     the router weight into registers.
-//  2. Router matvec on the tensor cores (routing.cuh), fp32 partial logits
-//     to the workspace, then a grid-wide barrier (bounded spin).
+//  2. Router matvec on the tensor cores (routing.cuh): fp32 partial logits
+//     to the call's buffer (odd or even call: the index comes from the
+//     arrival count the previous call left), the same words of the other
+//     buffer marked unwritten for the next call.  No grid-wide barrier
+//     follows: a reader polls the words it needs (bounded) until none is
+//     unwritten.
 //  3. EVERY CTA computes the top-k of all tokens and the compaction itself
-//     (shared memory only): nothing is published and re-read, no second
-//     launch, no last-CTA hand-off.  The results are bitwise equal in all
+//     (shared memory only): nothing else is published and re-read, no
+//     second launch, no last-CTA hand-off.  The results are bitwise equal in all
 //     CTAs (same inputs, same code), so they agree on every position.  With
 //     at most 16 tokens every chosen expert is one group and the compaction
 //     is worked out on the pair axis (two short loops, no scan).
@@ -96,6 +100,9 @@ static_assert(kOffCall + 8 <= kOffTile && kOffTile + 4 * kMaxGateUpStages <= kOf
                   kOffCells + 4 * kMaxDownStages * kConsumerWarps <= kRingOff,
               "map");
 static_assert(kRingOff % 128 == 0, "ring alignment");
+static_assert((unsigned long long)(kMaxPairs + kMaxTokens) * (2 * 32 * kMaxDownChunks / kGateUpTileRows) * 1024ull <
+                  (1ull << 32),
+              "static splits in 32-bit arithmetic (groups x tiles per group x grids of up to 1024 CTAs)");
 static_assert(kMaxGateUpStages < kRedSlots, "reduction slots must outnumber ring stages");
 
 struct OneSlab {  // a down cell of one slab, as a compile-time count
@@ -130,24 +137,6 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
   return v;
 }
 
-// Grid-wide arrival, called by ONE thread per CTA right after the threads
-// whose writes it publishes have synchronised with it (a CTA barrier or an
-// mbarrier): its fence makes those writes visible device-wide before it
-// arrives (one fence per CTA -- under full HBM load a fence from every
-// thread stalls the SM).  The 64-bit count is never reset: every use adds
-// exactly gridDim.x per call, so an arrival that returned `old` is complete
-// when the count reaches the next multiple of gridDim.x above it.  Returns
-// that target.
-__device__ __forceinline__ unsigned long long grid_arrive(unsigned* word) {
-  // release pattern: an acq_rel fence then the (relaxed) arrival; a
-  // sequentially consistent fence is not needed and costs far more while
-  // bulk copies are in flight
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-  const unsigned long long G = gridDim.x;
-  const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(word), 1ull);
-  return (old / G + 1ull) * G;
-}
-
 // Bounded acquire-spin until the count at `word` reaches `target`.
 __device__ inline bool grid_wait(const Workspace& ws, const unsigned* word, unsigned long long target,
                                  int phase) {
@@ -167,6 +156,10 @@ __device__ inline bool grid_wait(const Workspace& ws, const unsigned* word, unsi
 
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+// First tile of CTA c in a static split of T tiles: floor(T c / grid), in
+// 32-bit arithmetic (T <= kMaxPairs x 128 tiles, so T x grid < 2^32).
+__device__ __forceinline__ int static_share(int T, unsigned c) { return (int)((unsigned)T * c / gridDim.x); }
 
 }  // namespace layer_detail
 
@@ -259,38 +252,44 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   pdl_wait();               // x and the workspace belong to this call now
   pdl_launch_dependents();  // the next call's prologue may start as SMs free up
   if (tid == 0) stamp(a, 0);
+  if (warp == kPublisherWarp && lane == 0) {
+    // the previous call on this workspace is complete: its CTAs' arrivals
+    // give this call's index (acquire: nothing of this call moves above it)
+    const unsigned long long idx = ld_acquire64(reinterpret_cast<const unsigned long long*>(a.ws.sync + kSyncCount)) /
+                                       gridDim.x + 1ull;
+    *call_idx = idx;
+    if (blockIdx.x == 0) {  // the work counters of the next call (this call's were cleared by the last)
+      a.ws.sync[idx & 1ull ? kSyncGateUpNext : kSyncGateUpNextOdd] = 0u;
+      a.ws.sync[idx & 1ull ? kSyncDownNext : kSyncDownNextOdd] = 0u;
+    }
+  }
 
-  // ---- 2. router matvec, then every partial logit is published
+  // ---- 2. router matvec into this call's buffer of partial logits (no
+  // grid-wide barrier after it: the readers poll the words)
   const size_t plane = (size_t)kMaxTokens * a.E;
+  __syncthreads();  // the call index is in shared memory
+  const bool odd = (*call_idx & 1ull) != 0ull;
+  float* part = a.ws.part + (odd ? (size_t)a.ks * plane : 0);
+  float* part_next = a.ws.part + (odd ? 0 : (size_t)a.ks * plane);
   for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
     if (unit != (int)blockIdx.x) {
       gu = gemv_unit(unit, a.ks, a.H, gw);
       if (warp < kConsumerWarps) gemv_load_w<KPW>(a.w_router, a.E, a.H, gu, lane, wb);
     }
+    if (warp == kProducerWarp) gemv_clear(gu, kMaxTokens, a.E, plane, part_next, lane);
     for (int mb = 0; mb * 16 < a.M; ++mb) {
       if (warp < kConsumerWarps) red[warp * 32 + lane] = gemv_tokens<KPW>(a.x, a.M, a.H, gu, mb, lane, wb);
       __syncthreads();
-      if (warp == 0) gemv_store(red, gu, mb, a.M, a.E, plane, a.ws.part, lane);
+      if (warp == 0) gemv_store<true>(red, gu, mb, a.M, a.E, plane, part, lane);
       __syncthreads();
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    stamp(a, 1);
-    if (blockIdx.x == 0) {  // the per-call work counters; nothing reads them before the barrier
-      a.ws.sync[kSyncGateUpNext] = 0u;
-      a.ws.sync[kSyncDownNext] = 0u;
-    }
-    const unsigned long long t1 = grid_arrive(a.ws.sync + kSyncCount);
-    grid_wait(a.ws, a.ws.sync + kSyncCount, t1, 1);
-    *call_idx = (t1 / gridDim.x + 1ull) / 2ull;  // two barrier arrivals per CTA per call
-    stamp(a, 2);
-  }
-  __syncthreads();
+  if (tid == 0) stamp(a, 1);
 
   // ---- 3. top-k of every token, compaction (every CTA, shared memory only)
   for (int m = warp; m < a.M; m += kExpertThreads / 32) {
-    const float w = topk_dispatch(a.ws.part + (size_t)m * a.E, plane, a.ks, a.bias, a.E, a.K, lane,
+    const float w = topk_dispatch(PolledPlanes{part + (size_t)m * a.E, plane}, a.ks, a.bias, a.E, a.K, lane,
                                   a.ws.status, rt.s_e + m * a.K, VARIANT && a.sel_only != 0);
     __syncwarp();
     if (lane < a.K) {
@@ -313,7 +312,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   __syncthreads();
   if (tid == 0) stamp(a, 12);
   // the reduction area is free until the gate/up loop: scratch for the
-  // pair-axis compaction
+  // pair-axis compaction (small loops: this code runs once per call, with a
+  // cold instruction cache, so its size costs more than its arithmetic)
   const int n_groups = a.M <= kGroupTokens
                            ? compact_pairs(rt, NP, a.K, MK, reinterpret_cast<int*>(red), tid, kExpertThreads)
                            : (compact_masks(rt, NP, a.K, MK, EA), rt.scal[0]);
@@ -392,14 +392,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     unsigned long long waited = 0;
     // static share of each phase, then single tiles from the shared tail
     const int Ts = g_static * TPG;
-    const int s0 = (int)((long long)Ts * blockIdx.x / gridDim.x);
-    const int s1 = (int)((long long)Ts * (blockIdx.x + 1) / gridDim.x);
+    const int s0 = static_share(Ts, blockIdx.x), s1 = static_share(Ts, blockIdx.x + 1);
     const int Ts2 = g_static * SPG;
-    const int q0 = (int)((long long)Ts2 * blockIdx.x / gridDim.x);
-    const int q1 = (int)((long long)Ts2 * (blockIdx.x + 1) / gridDim.x);
-    unsigned* next_gu = a.ws.sync + kSyncGateUpNext;
+    const int q0 = static_share(Ts2, blockIdx.x), q1 = static_share(Ts2, blockIdx.x + 1);
+    unsigned* next_gu = a.ws.sync + (odd ? kSyncGateUpNextOdd : kSyncGateUpNext);
     const uint64_t wpol = l2_evict_first_policy();  // expert weights: read once per call
-    unsigned* next_d = a.ws.sync + kSyncDownNext;
+    unsigned* next_d = a.ws.sync + (odd ? kSyncDownNextOdd : kSyncDownNext);
     // gate/up tiles of the shared tail are taken one ahead (the atomic's
     // round trip hides behind a tile), starting one tile before the static
     // share ends: a tile taken earlier would be held back from faster SMs.
@@ -576,8 +574,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     // this CTA's statically split tiles come first: after the last of them
     // (or at once if it has none) the warp reports them reduced
     const int Ts = g_static * TPG;
-    const int n_static = (int)((long long)Ts * (blockIdx.x + 1) / gridDim.x) -
-                         (int)((long long)Ts * blockIdx.x / gridDim.x);
+    const int n_static = static_share(Ts, blockIdx.x + 1) - static_share(Ts, blockIdx.x);
     if (n_static == 0 && lane == 0) mbar_arrive(static_bar);
     for (int j = 0;; ++j) {
       const int s = j % S;
@@ -903,18 +900,22 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   }
 
   // ---- 6. every CTA's weighted rows written -> combine.  Only the first
-  // n_own_ctas CTAs combine (8 output slabs each: CTA c owns 8c .. 8c+7):
+  // n_own_ctas CTAs combine (3 output slabs each: CTA c owns 3c .. 3c+2):
   // each token's k rows summed in slot order, ONE bf16 rounding.  The other
   // CTAs count themselves in and leave at once, so the next call's CTAs get
-  // their SMs (and run their prologue) while the combine runs.
+  // their SMs (and run their prologue) while the combine runs.  (Three slabs
+  // a CTA measured faster than eight: the combine is a latency-bound read
+  // of L2, so more CTAs end it sooner, and at hidden 2560 about 45 SMs are
+  // still left to the next call's prologue.)
   const int SLc = a.H / kDownTileRows;  // 8-row output slabs of the combine
-  const int n_own_ctas = min((int)gridDim.x, (SLc + kConsumerWarps - 1) / kConsumerWarps);
-  const int own_per = (SLc + n_own_ctas - 1) / n_own_ctas;  // 8 unless the grid is small
+  constexpr int kCombineSlabs = 3;
+  const int n_own_ctas = min((int)gridDim.x, (SLc + kCombineSlabs - 1) / kCombineSlabs);
+  const int own_per = (SLc + n_own_ctas - 1) / n_own_ctas;  // kCombineSlabs unless the grid is small
   const bool owner = (int)blockIdx.x < n_own_ctas;
   consumers_sync();
   if (tid == 0) {
     grid_count(a.ws.sync + kSyncCount);
-    if (owner) grid_wait(a.ws, a.ws.sync + kSyncCount, 2ull * *call_idx * gridDim.x, 3);
+    if (owner) grid_wait(a.ws, a.ws.sync + kSyncCount, *call_idx * gridDim.x, 3);
   }
   if (!owner) return;
   consumers_sync();

@@ -356,7 +356,8 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
   const size_t o_status = take(4), o_diag = take(32), o_sync = take(kSyncWords * 4);
-  const size_t o_part = take((size_t)h->ks * kMaxTokens * E * 4);
+  const size_t part_bytes = 2 * (size_t)h->ks * kMaxTokens * E * 4;  // odd and even calls
+  const size_t o_part = take(part_bytes);
   const size_t o_ng = take(4), o_na = take(4);
   const size_t o_ge = take(np * 4), o_gs = take(np * 4), o_gc = take(np * 4);
   const size_t o_pl = take(np * 4), o_pw = take(np * 4);
@@ -394,6 +395,7 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   }
   h->cap_stream = s;
   bool ok = cudaMemsetAsync(h->ws_mem, 0, h->ws_bytes, s) == cudaSuccess &&
+            cudaMemsetAsync(h->ws.part, 0xff, part_bytes, s) == cudaSuccess &&  // every logit unwritten
             cudaMemcpyAsync(h->w_router, w_router, b_router, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
   if (ok && fp8) {
     pack_gate_up_fp8(static_cast<const uint8_t*>(w_gate_up), h->w_gu, n_experts, inter, hidden, s);
@@ -553,9 +555,11 @@ int moe_get_status(moe_layer_t* h) {
   if (st) {
     cudaMemset(h->ws.status, 0, 4);
     cudaMemset(h->ws.diag, 0, sizeof dg);
-    // a wait that gave up may have left the grid-barrier count between two
-    // multiples of the grid: start it again from zero (no kernel runs now)
+    // a wait that gave up may have left the arrival counts between two
+    // multiples of the grid: start them again from zero (no kernel runs
+    // now), with every partial logit of both buffers unwritten again
     cudaMemset(h->ws.sync, 0, kSyncWords * 4);
+    cudaMemset(h->ws.part, 0xff, 2 * (size_t)h->ks * kMaxTokens * h->E * 4);
     set_err("device status bits 0x%x (1 stage wait, 2 free-stage wait, 4 reduction wait, 8 no top-k "
             "candidate, 16 grid-wide wait); first timeout: phase %llu kind %llu cta %llu stages %llu "
             "index %llu waited %llu ns barrier 0x%016llx thread %llu grid %llu",

@@ -77,8 +77,8 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) route_kernel(RouteArgs a)
   __threadfence();
   for (int m = warp; m < a.M; m += kConsumerWarps) {
     // the lane holding each slot writes its expert id straight to the output
-    const float w = topk_dispatch(a.part + (size_t)m * a.E, plane, a.ks, a.bias, a.E, a.K, lane, a.status,
-                                  a.topk_idx + m * a.K);
+    const float w = topk_dispatch(PlainPlanes{a.part + (size_t)m * a.E, plane}, a.ks, a.bias, a.E, a.K, lane,
+                                  a.status, a.topk_idx + m * a.K);
     if (lane < a.K && a.topk_w) a.topk_w[m * a.K + lane] = w;
   }
   if (threadIdx.x == 0) *a.counter = 0u;  // ready for the next call

@@ -24,6 +24,12 @@
 //    operand row per chunk (the same permutation on A and B leaves every dot
 //    product unchanged).  Units write fp32 partial logits; the reader sums
 //    the ks partials in a fixed order, so the logits are deterministic.
+//    Inside the layer kernel the partial logits live in two buffers used by
+//    odd and even calls; a call's units write theirs into the call's buffer
+//    and set the same words of the other buffer to an "unwritten" bit
+//    pattern (a NaN that no arithmetic produces).  A reader polls the words
+//    it needs until none is unwritten, so no grid-wide barrier (and no flag
+//    round trip) sits between the matvec and the top-k.
 //  * Top-k, one warp per token: the E logits sit in registers (lane l holds
 //    experts l + 32v as order-preserving integer keys).  Every lane first
 //    lists its two best keys (a max/min tree, then the lowest positions
@@ -98,8 +104,23 @@ __device__ __forceinline__ float4 gemv_tokens(const __nv_bfloat16* __restrict__ 
   return make_float4(c0[0] + c1[0], c0[1] + c1[1], c0[2] + c1[2], c0[3] + c1[3]);
 }
 
+// A partial logit that is not written yet (never produced by arithmetic:
+// the hardware's NaN results are positive).
+constexpr uint32_t kUnwritten = 0xffffffffu;
+
+// One partial logit: a plain store (read after a fence and a counter), or a
+// relaxed gpu-scope store (read by other CTAs polling the word).
+template <bool kPolled>
+__device__ __forceinline__ void put_logit(float* P, size_t i, float v) {
+  if constexpr (kPolled)
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(P + i), "f"(v) : "memory");
+  else
+    P[i] = v;
+}
+
 // Warp 0 of the unit's CTA: sum the 8 warp partials in warp order and store
 // the unit's fp32 partial logits part[kc][m][e] (plane = rows * E floats).
+template <bool kPolled = false>
 __device__ __forceinline__ void gemv_store(const float4* red, const GemvUnit& u, int mb, int M, int E,
                                            size_t plane, float* __restrict__ part, int lane) {
   float4 s = red[lane];
@@ -115,12 +136,24 @@ __device__ __forceinline__ void gemv_store(const float4* red, const GemvUnit& u,
   const int m0 = mb * 16 + (lane >> 2), m1 = m0 + 8;
   float* P = part + (size_t)u.kc * plane;
   if (m0 < M) {
-    if (e < E) P[(size_t)m0 * E + e] = s.x;
-    if (e + 1 < E) P[(size_t)m0 * E + e + 1] = s.y;
+    if (e < E) put_logit<kPolled>(P, (size_t)m0 * E + e, s.x);
+    if (e + 1 < E) put_logit<kPolled>(P, (size_t)m0 * E + e + 1, s.y);
   }
   if (m1 < M) {
-    if (e < E) P[(size_t)m1 * E + e] = s.z;
-    if (e + 1 < E) P[(size_t)m1 * E + e + 1] = s.w;
+    if (e < E) put_logit<kPolled>(P, (size_t)m1 * E + e, s.z);
+    if (e + 1 < E) put_logit<kPolled>(P, (size_t)m1 * E + e + 1, s.w);
+  }
+}
+
+// One warp: mark the unit's words of ALL rows (tokens) of the other
+// buffer unwritten, ready for the next call (whatever its M).
+__device__ __forceinline__ void gemv_clear(const GemvUnit& u, int rows, int E, size_t plane,
+                                           float* __restrict__ part, int lane) {
+  float* P = part + (size_t)u.kc * plane + u.tile * 8;
+  const int n = min(8, E - u.tile * 8);
+  for (int i = lane; i < rows * 8; i += 32) {
+    const int m = i >> 3, c = i & 7;
+    if (c < n) P[(size_t)m * E + c] = __uint_as_float(kUnwritten);
   }
 }
 
@@ -192,40 +225,123 @@ __device__ __forceinline__ void top2_below(const uint32_t (&key)[VPL], uint32_t 
   v2 = k2 == 0u ? VPL : __ffs(m2) - 1;
 }
 
-// Top-k of one token by one warp.  lg: the token's partial logits (plane 0;
-// ks planes `plane` floats apart), summed in plane order, plus the bias.
+// Sources of one token's partial logits (ks planes, `plane` words apart).
+// sum(): lane l gets the fp32 sum over the planes, in plane order, of the
+// logits of experts l + 32 v (0 past E).  one(): the same sum for one expert.
+struct PlainPlanes {  // fp32 words, complete before the reader starts
+  const float* lg;
+  size_t plane;
+  template <int VPL>
+  __device__ __forceinline__ void sum(int lane, int E, int ks, float (&lv)[VPL], int*) const {
+    float l1[VPL];  // planes 0 and 1 in one round trip, further planes one each
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const int e = v * 32 + lane;
+      lv[v] = e < E ? __ldcg(lg + e) : 0.f;
+      l1[v] = (ks > 1 && e < E) ? __ldcg(lg + plane + e) : 0.f;
+    }
+    if (ks > 1) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) lv[v] += l1[v];
+    }
+    for (int c = 2; c < ks; ++c) {
+      float pv[VPL];
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const int e = v * 32 + lane;
+        pv[v] = e < E ? __ldcg(lg + (size_t)c * plane + e) : 0.f;
+      }
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) lv[v] += pv[v];
+    }
+  }
+  __device__ __forceinline__ float one(int e, int ks) const {
+    float l = __ldcg(lg + e);
+    for (int c = 1; c < ks; ++c) l += __ldcg(lg + (size_t)c * plane + e);
+    return l;
+  }
+};
+
+__device__ __forceinline__ uint32_t ld_relaxed32(const float* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Words written by other CTAs of the same call while this warp reads them:
+// every word still unwritten is re-read until none is (bounded: after
+// kWaitTimeoutNs the status gets kErrTimeoutGrid and the call's result is
+// undefined).  Planes 0 and 1 are polled together, further planes one each.
+struct PolledPlanes {
+  const float* lg;
+  size_t plane;
+  template <int VPL>
+  __device__ __forceinline__ void poll(const float* P, const float* Q, int lane, int E, uint32_t (&w0)[VPL],
+                                       uint32_t (&w1)[VPL], int* status) const {
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const int e = v * 32 + lane;
+      w0[v] = e < E ? ld_relaxed32(P + e) : 0u;
+      w1[v] = (Q && e < E) ? ld_relaxed32(Q + e) : 0u;
+    }
+    unsigned long long t0 = 0ull;
+    for (int it = 0;; ++it) {
+      bool ok = true;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) ok = ok && w0[v] != kUnwritten && w1[v] != kUnwritten;
+      if (__all_sync(0xffffffffu, ok)) return;
+      if (it == 0) {
+        t0 = global_timer_ns();
+      } else if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (lane == 0) set_error(status, kErrTimeoutGrid);
+        return;
+      }
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const int e = v * 32 + lane;
+        if (w0[v] == kUnwritten) w0[v] = ld_relaxed32(P + e);
+        if (w1[v] == kUnwritten) w1[v] = ld_relaxed32(Q + e);
+      }
+    }
+  }
+  template <int VPL>
+  __device__ __forceinline__ void sum(int lane, int E, int ks, float (&lv)[VPL], int* status) const {
+    uint32_t w0[VPL], w1[VPL];
+    poll<VPL>(lg, ks > 1 ? lg + plane : nullptr, lane, E, w0, w1, status);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      lv[v] = __uint_as_float(w0[v]);  // 0 past E
+      if (ks > 1) lv[v] += __uint_as_float(w1[v]);
+    }
+    for (int c = 2; c < ks; ++c) {
+      poll<VPL>(lg + (size_t)c * plane, nullptr, lane, E, w0, w1, status);
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) lv[v] += __uint_as_float(w0[v]);
+    }
+  }
+  __device__ __forceinline__ float one(int e, int ks) const {  // words already seen written
+    float l = __uint_as_float(ld_relaxed32(lg + e));
+    for (int c = 1; c < ks; ++c) l += __uint_as_float(ld_relaxed32(lg + (size_t)c * plane + e));
+    return l;
+  }
+};
+
+// Top-k of one token by one warp.  src: the token's partial logits, summed
+// in plane order, plus the bias.
 // Lane j < K writes slot j's expert id to idx_out[j] (the caller reads them
 // after a __syncwarp) and returns slot j's renormalised weight; the other
 // lanes return 0.  sel_only: the bias picks the experts only, the weights
 // come from the unbiased logits (re-read for the k chosen experts).
-template <int VPL>
-__device__ __forceinline__ float topk_token(const float* __restrict__ lg, size_t plane, int ks,
-                                            const float* __restrict__ bias, int E, int K, int lane,
-                                            int* status, int* idx_out, bool sel_only) {
-  // planes 0 and 1 and the bias in one round trip; further planes one each;
-  // the sum order is plane 0, 1, ..., then the bias
-  float lv[VPL], l1[VPL], bv_[VPL];
+template <int VPL, class Src>
+__device__ __forceinline__ float topk_token(const Src& src, int ks, const float* __restrict__ bias, int E, int K,
+                                            int lane, int* status, int* idx_out, bool sel_only) {
+  float lv[VPL], bv_[VPL];
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = v * 32 + lane;
-    lv[v] = e < E ? __ldcg(lg + e) : 0.f;
-    l1[v] = (ks > 1 && e < E) ? __ldcg(lg + plane + e) : 0.f;
     bv_[v] = (bias && e < E) ? __ldg(bias + e) : 0.f;
   }
-  if (ks > 1) {
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) lv[v] += l1[v];
-  }
-  for (int c = 2; c < ks; ++c) {
-    float pv[VPL];
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      const int e = v * 32 + lane;
-      pv[v] = e < E ? __ldcg(lg + (size_t)c * plane + e) : 0.f;
-    }
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) lv[v] += pv[v];
-  }
+  src.template sum<VPL>(lane, E, ks, lv, status);
   uint32_t key[VPL];
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
@@ -266,10 +382,7 @@ __device__ __forceinline__ float topk_token(const float* __restrict__ lg, size_t
   float my_val = key_value(my_key), ref_val = key_value(top0);
   if (sel_only && bias) {  // the unbiased logits of the chosen, summed as above
     float l = 0.f;
-    if (lane < K) {
-      l = __ldcg(lg + my_win);
-      for (int c = 1; c < ks; ++c) l += __ldcg(lg + (size_t)c * plane + my_win);
-    }
+    if (lane < K) l = src.one((int)my_win, ks);
     my_val = l;
     ref_val = key_value(__reduce_max_sync(0xffffffffu, lane < K ? ordered_key(l) : 0u));
   }
@@ -279,15 +392,15 @@ __device__ __forceinline__ float topk_token(const float* __restrict__ lg, size_t
   return lane < K ? __fdividef(ex, s) : 0.f;
 }
 
-__device__ __forceinline__ float topk_dispatch(const float* lg, size_t plane, int ks, const float* bias,
-                                               int E, int K, int lane, int* status, int* idx_out,
-                                               bool sel_only = false) {
-  if (E <= 32) return topk_token<1>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
-  if (E <= 64) return topk_token<2>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
-  if (E <= 128) return topk_token<4>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
-  if (E <= 256) return topk_token<8>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
-  if (E <= 512) return topk_token<16>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
-  return topk_token<32>(lg, plane, ks, bias, E, K, lane, status, idx_out, sel_only);
+template <class Src>
+__device__ __forceinline__ float topk_dispatch(const Src& src, int ks, const float* bias, int E, int K, int lane,
+                                               int* status, int* idx_out, bool sel_only = false) {
+  if (E <= 32) return topk_token<1>(src, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 64) return topk_token<2>(src, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 128) return topk_token<4>(src, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 256) return topk_token<8>(src, ks, bias, E, K, lane, status, idx_out, sel_only);
+  if (E <= 512) return topk_token<16>(src, ks, bias, E, K, lane, status, idx_out, sel_only);
+  return topk_token<32>(src, ks, bias, E, K, lane, status, idx_out, sel_only);
 }
 
 // ------------------------------------------------------- compaction ----
