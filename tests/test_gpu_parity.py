@@ -285,6 +285,30 @@ def test_graph_capture_by_caller(ling):
             assert torch.equal(o, r)
 
 
+def test_back_to_back_calls_with_changing_M(ling):
+    """Calls chained on one stream (PDL, no host synchronisation) while M
+    changes from call to call.  Each call reads the partial logits of the
+    buffer its parity (odd / even call) picks, which the call before marked
+    unwritten for all 64 token rows, so a call with more tokens than the one
+    two calls earlier never takes a stale row (16 -> 1 -> 16, 2 -> 64).
+    Every result equals the same call made alone."""
+    layer, _ = ling
+    layer.set_router_bias(None)
+    Ms = [16, 1, 16, 6, 64, 2, 64, 1, 6]
+    xs = [wl.tokens(M, wl.LING.hidden, seed=900_000 + i, device=DEV) for i, M in enumerate(Ms)]
+    alone = []
+    for x in xs:
+        out, idx = layer(x)
+        torch.cuda.synchronize()
+        alone.append((out.clone(), idx.clone()))
+    chained = [layer(x) for x in xs]
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    for n, ((o, i), (ro, ri)) in enumerate(zip(chained, alone)):
+        assert torch.equal(i, ri), f"call {n} (M = {Ms[n]}): expert ids differ"
+        assert torch.equal(o.view(torch.int16), ro.view(torch.int16)), f"call {n} (M = {Ms[n]}): outputs differ"
+
+
 def test_swiglu_epilogue_full_range(oracle, MoELayer):
     """Every finite bf16 gate value through the fused epilogue.
 
