@@ -18,6 +18,7 @@ with a barrier and a device synchronize on both sides; max over ranks.
     python bench.py --impl reference     # the CPU oracle on the same workload
     python bench.py --sweep               # M x routing sweep (writes JSON lines)
     python bench.py --lm-head [--M 1]     # the bf16 vocabulary projection
+    python bench.py --crossover           # the contraction on CUDA cores vs tensor cores, M_e = 1..16
 """
 from __future__ import annotations
 
@@ -617,6 +618,74 @@ def run_sweep(args):
     wkl.close()
 
 
+def run_crossover(args):
+    """The expert contraction on the CUDA cores and on the tensor cores
+    (include/gemv.h) over the layer's packed tiles: one launch streams the
+    gate/up rows (k = hidden) or the down rows (k = inter) of 46 experts --
+    the distinct experts of an M = 6 call -- for M_e tokens; 4 distinct
+    weight sets (about 1 GB) are cycled so every call reads from HBM.  One
+    JSON line per (shape, M_e, engine), then one per shape with the
+    crossover: the smallest M_e from which the tensor cores are faster."""
+    import torch
+    from weight_streaming_expert_gb300 import gemv as G
+    from weight_streaming_expert_gb300 import workloads as wl
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    shape = wl.SHAPES[args.shape]
+    H, I, A, n_sets = shape.hidden, shape.inter, 46, 4
+    peak, peak_kind = measured_peaks()
+    Ms = (1, 2, 3, 4, 6, 8, 12, 16)
+    for name, rows, k in (("gate_up", A * 2 * I, H), ("down", A * H, I)):
+        gen = torch.Generator(device=dev).manual_seed(4242 + rows)
+        packs = []
+        for _ in range(n_sets):
+            w = (torch.randn(rows, k, generator=gen, device=dev) * wl.WEIGHT_STD).to(torch.bfloat16)
+            packs.append(G.pack(w))
+            del w
+        torch.cuda.empty_cache()
+        res = {}
+        for M in Ms:
+            xs = [wl.tokens(M, k, seed=7_000_000 + i, device=dev) for i in range(n_sets)]
+            ys = [torch.empty((M, rows), dtype=torch.float32, device=dev) for _ in range(n_sets)]
+            for eng_name, eng in (("cuda_cores", G.CUDA_CORES), ("tensor_cores", G.TENSOR_CORES)):
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                n = max(n_sets, min(args.steps, 256) // n_sets * n_sets)
+                with torch.cuda.stream(s):
+                    for c in range(max(args.warmup, n_sets)):
+                        G.gemv(packs[c % n_sets], xs[c % n_sets], eng, ys[c % n_sets], stream=s)
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=s):
+                        for c in range(n):
+                            G.gemv(packs[c % n_sets], xs[c % n_sets], eng, ys[c % n_sets], stream=s)
+                    g.replay()
+                s.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                with torch.cuda.stream(s):
+                    e0.record(s)
+                    g.replay()
+                    e1.record(s)
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1000.0 / n
+                b = rows * k * 2 + M * k * 2 + M * rows * 4
+                gbs = b / (us * 1e-6) / 1e9
+                res[(M, eng_name)] = us
+                print(json.dumps({"crossover": True, "shape": f"{name} ({A} experts: {rows} x {k} bf16)", "M_e": M,
+                                  "engine": eng_name, "us_per_call": round(us, 3), "achieved_gbs": round(gbs, 1),
+                                  "frac_of_peak": round(gbs / peak, 4), "peak_kind": peak_kind,
+                                  "weight_sets_cycled": n_sets, "calls": n}), flush=True)
+        tc_wins = [M for M in Ms if res[(M, "tensor_cores")] < 0.97 * res[(M, "cuda_cores")]]
+        cc_wins = [M for M in Ms if res[(M, "cuda_cores")] < 0.97 * res[(M, "tensor_cores")]]
+        print(json.dumps({"crossover_summary": True, "shape": name,
+                          "tensor_cores_faster_from_M_e": min(tc_wins) if tc_wins else None,
+                          "cuda_cores_faster_at_M_e": cc_wins,
+                          "ratio_cuda_over_tensor": {str(M): round(res[(M, "cuda_cores")] / res[(M, "tensor_cores")], 3)
+                                                     for M in Ms}}), flush=True)
+        del packs
+        torch.cuda.empty_cache()
+
+
 def run_lm_head(args):
     """The vocabulary projection (include/lm_head.h), timed like the layer:
     calls captured into CUDA graphs (PDL intact), two distinct weight copies
@@ -721,6 +790,8 @@ def main(argv=None):
     ap.add_argument("--fp8", action="store_true", help="layers with fp8 (E4M3) expert weights and row scales")
     ap.add_argument("--variant", action="store_true",
                     help="layers with a shared expert, routed scale 2.5 and the router bias for selection only")
+    ap.add_argument("--crossover", action="store_true",
+                    help="the expert contraction on CUDA cores vs tensor cores over M_e = 1..16 (JSON lines)")
     ap.add_argument("--lm-head", dest="lm_head", action="store_true",
                     help="time the bf16 vocabulary projection (hidden 2560, vocab 157,184; M <= 16) instead")
     args = ap.parse_args(argv)
@@ -732,6 +803,8 @@ def main(argv=None):
         run_lm_head(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.crossover:
+        run_crossover(args)
     else:
         run_ours(args)
 

@@ -107,3 +107,25 @@ def test_lm_head_forward_rejects_null_handle(L):
     assert L.moe_lm_head_forward(None, None, None, 1, None) == native.MOE_ERR_INVALID_ARG
     assert L.moe_lm_head_get_status(None) == native.MOE_ERR_INVALID_ARG
     L.moe_lm_head_destroy(None)  # no-op
+
+
+@pytest.mark.parametrize("rows,k,M,engine,status,frag", [
+    (12, 256, 1, 0, native.MOE_ERR_INVALID_ARG, "rows"),    # rows not a multiple of 8
+    (16, 288, 1, 0, native.MOE_ERR_INVALID_ARG, "k ="),     # k not a multiple of 256
+    (16, 3328, 1, 1, native.MOE_ERR_INVALID_ARG, "k ="),    # k above 3072
+    (16, 256, 1, 5, native.MOE_ERR_INVALID_ARG, "engine"),
+    (16, 256, -1, 0, native.MOE_ERR_INVALID_ARG, "M ="),
+    (16, 256, 17, 1, native.MOE_ERR_UNSUPPORTED, "exceeds"),
+    (16, 256, 2, 1, native.MOE_ERR_INVALID_ARG, "aligned"),  # null pointers
+])
+def test_gemv_rejects_bad_arguments_before_the_gpu(L, rows, k, M, engine, status, frag):
+    assert L.moe_gemv(None, None, None, rows, k, M, engine, None) == status
+    assert frag in native.last_error()
+
+
+def test_gemv_zero_tokens_and_pack_checks(L):
+    assert L.moe_gemv(None, None, None, 16, 256, 0, 0, None) == native.MOE_OK
+    assert L.moe_gemv_pack(None, None, 16, 64, None) == native.MOE_ERR_INVALID_ARG
+    assert L.moe_gemv_pack(ctypes.c_void_p(24), ctypes.c_void_p(32), 16, 64, None) == native.MOE_ERR_INVALID_ARG
+    assert "aligned" in native.last_error()
+    assert L.moe_gemv_pack(ctypes.c_void_p(16), ctypes.c_void_p(32), 15, 64, None) == native.MOE_ERR_INVALID_ARG

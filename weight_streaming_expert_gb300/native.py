@@ -24,6 +24,9 @@ MOE_ERR_OOM = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
 MOE_MAX_TOKENS = 64
 MOE_LM_HEAD_MAX_TOKENS = 16
+MOE_GEMV_MAX_TOKENS = 16
+MOE_GEMV_CUDA_CORES = 0
+MOE_GEMV_TENSOR_CORES = 1
 MOE_FWD_NO_PDL = 0x1
 MOE_FWD_GRAPH = 0x2
 MOE_FWD_TRACE = 0x4
@@ -110,6 +113,12 @@ def lib(build_if_missing: bool = True):
         L.moe_lm_head_get_status.restype = ci
         L.moe_lm_head_destroy.argtypes = [vp]
         L.moe_lm_head_destroy.restype = None
+        L.moe_gemv_pack.argtypes = [vp, vp, ci, ci, vp]
+        L.moe_gemv_pack.restype = ci
+        L.moe_gemv.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+        L.moe_gemv.restype = ci
+        L.moe_gemv_get_status.argtypes = []
+        L.moe_gemv_get_status.restype = ci
         L.moe_last_error.argtypes = []
         L.moe_last_error.restype = ctypes.c_char_p
         _lib = L
