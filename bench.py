@@ -634,8 +634,9 @@ def run_crossover(args):
     shape = wl.SHAPES[args.shape]
     H, I, A, n_sets = shape.hidden, shape.inter, 46, 4
     peak, peak_kind = measured_peaks()
-    Ms = (1, 2, 3, 4, 6, 8, 12, 16)
-    for name, rows, k in (("gate_up", A * 2 * I, H), ("down", A * H, I)):
+    Ms = tuple(args.crossover_m) if args.crossover_m else (1, 2, 3, 4, 6, 8, 12, 16)
+    shapes = (("gate_up", A * 2 * I, H), ("down", A * H, I))
+    for name, rows, k in (s_ for s_ in shapes if args.crossover_shape in ("both", s_[0])):
         gen = torch.Generator(device=dev).manual_seed(4242 + rows)
         packs = []
         for _ in range(n_sets):
@@ -792,6 +793,9 @@ def main(argv=None):
                     help="layers with a shared expert, routed scale 2.5 and the router bias for selection only")
     ap.add_argument("--crossover", action="store_true",
                     help="the expert contraction on CUDA cores vs tensor cores over M_e = 1..16 (JSON lines)")
+    ap.add_argument("--crossover-m", dest="crossover_m", type=int, nargs="+", default=None,
+                    help="--crossover: the token counts M_e to time (default 1 2 3 4 6 8 12 16)")
+    ap.add_argument("--crossover-shape", dest="crossover_shape", choices=["both", "gate_up", "down"], default="both")
     ap.add_argument("--lm-head", dest="lm_head", action="store_true",
                     help="time the bf16 vocabulary projection (hidden 2560, vocab 157,184; M <= 16) instead")
     args = ap.parse_args(argv)
