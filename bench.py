@@ -618,6 +618,23 @@ def run_sweep(args):
     wkl.close()
 
 
+def crossover_summary(res, Ms, margin=0.03):
+    """res[(M_e, engine)] = us per call.  The smallest M_e from which the
+    tensor cores are faster by more than `margin` at every larger M_e too
+    (None if never), the M_e at which the CUDA cores are faster by more than
+    `margin`, and the time ratio CUDA / tensor per M_e."""
+    Ms = sorted(Ms)
+    tc = [M for M in Ms if res[(M, "tensor_cores")] < (1.0 - margin) * res[(M, "cuda_cores")]]
+    cross = None
+    for i, M in enumerate(Ms):
+        if all(m in tc for m in Ms[i:]):
+            cross = M
+            break
+    return {"tensor_cores_faster_from_M_e": cross,
+            "cuda_cores_faster_at_M_e": [M for M in Ms if res[(M, "cuda_cores")] < (1.0 - margin) * res[(M, "tensor_cores")]],
+            "ratio_cuda_over_tensor": {str(M): round(res[(M, "cuda_cores")] / res[(M, "tensor_cores")], 3) for M in Ms}}
+
+
 def run_crossover(args):
     """The expert contraction on the CUDA cores and on the tensor cores
     (include/gemv.h) over the layer's packed tiles: one launch streams the
@@ -676,13 +693,7 @@ def run_crossover(args):
                                   "engine": eng_name, "us_per_call": round(us, 3), "achieved_gbs": round(gbs, 1),
                                   "frac_of_peak": round(gbs / peak, 4), "peak_kind": peak_kind,
                                   "weight_sets_cycled": n_sets, "calls": n}), flush=True)
-        tc_wins = [M for M in Ms if res[(M, "tensor_cores")] < 0.97 * res[(M, "cuda_cores")]]
-        cc_wins = [M for M in Ms if res[(M, "cuda_cores")] < 0.97 * res[(M, "tensor_cores")]]
-        print(json.dumps({"crossover_summary": True, "shape": name,
-                          "tensor_cores_faster_from_M_e": min(tc_wins) if tc_wins else None,
-                          "cuda_cores_faster_at_M_e": cc_wins,
-                          "ratio_cuda_over_tensor": {str(M): round(res[(M, "cuda_cores")] / res[(M, "tensor_cores")], 3)
-                                                     for M in Ms}}), flush=True)
+        print(json.dumps(dict(crossover_summary=True, shape=name, **crossover_summary(res, Ms))), flush=True)
         del packs
         torch.cuda.empty_cache()
 

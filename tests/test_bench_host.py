@@ -104,3 +104,18 @@ def test_reference_arm_prints_one_json_line(tmp_path):
     from weight_streaming_expert_gb300 import workloads as wl
     us, n, host = bench.oracle_call_us(wl.TINY, M=6, zipf=False, budget_s=0.5, max_calls=5)
     assert us > 0 and 1 <= n <= 5
+
+
+def test_crossover_summary_finds_the_first_lasting_tensor_core_win():
+    import bench
+    Ms = (1, 2, 3, 4)
+    res = {(1, "cuda_cores"): 9.6, (1, "tensor_cores"): 10.0,   # CUDA cores 4 % faster
+           (2, "cuda_cores"): 10.0, (2, "tensor_cores"): 9.8,   # within the margin
+           (3, "cuda_cores"): 12.0, (3, "tensor_cores"): 10.0,
+           (4, "cuda_cores"): 14.0, (4, "tensor_cores"): 10.0}
+    s = bench.crossover_summary(res, Ms)
+    assert s["tensor_cores_faster_from_M_e"] == 3
+    assert s["cuda_cores_faster_at_M_e"] == [1]
+    assert s["ratio_cuda_over_tensor"]["4"] == 1.4
+    res[(4, "tensor_cores")] = 14.0  # a tie at the largest M_e: no lasting win
+    assert bench.crossover_summary(res, Ms)["tensor_cores_faster_from_M_e"] is None
