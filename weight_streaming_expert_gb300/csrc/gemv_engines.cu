@@ -19,8 +19,8 @@
 // each warp with a private two-slot ring of 4 KB stages (8 chunks) in shared
 // memory filled by bulk copies on an mbarrier (lane 0 issues; plain loads
 // from every warp cannot keep enough bytes in flight to reach the HBM rate:
-// measured 29 % of peak).  The tokens sit in shared memory too (rows padded
-// by 16 bytes).  Only the arithmetic differs:
+// measured 29 % of peak).  The tokens sit in shared memory too (padded rows).
+// Only the arithmetic differs:
 //  * CUDA cores: the tokens are staged as fp32 when they fit (a token then
 //    costs two 16-byte shared loads and 8 FMAs per chunk), else as bf16
 //    (one load, 8 shifts, 8 FMAs); the lane's 8 weights become fp32 once per
@@ -48,6 +48,12 @@ constexpr int kStageChunks = 8;                        // chunks per stage
 constexpr uint32_t kStageBytes = kStageChunks * 512;  // 4 KB
 constexpr size_t kRingBytes = (size_t)kGemvWarps * 2 * kStageBytes;
 constexpr size_t kSmemLimit = 227 * 1024;
+// Token-row padding.  bf16 rows: k * 2 is a multiple of 512 (k % 256 == 0),
+// so a 64-byte pad puts rows g and g + 1 in opposite halves of the 32 banks
+// and a quarter-warp's 16-byte fragment loads (rows 2p, 2p + 1, 64 bytes
+// each) are conflict-free.  fp32 rows are read by broadcast (every lane of a
+// quarter-warp in one row): any 16-byte pad will do.
+constexpr int kPadBf16 = 64, kPadF32 = 16;
 
 __device__ int g_gemv_status;  // sticky: a bounded wait ran out
 
@@ -59,7 +65,7 @@ struct GemvArgs {
 };
 
 // Shared-memory token rows: MB rows of K values (bf16, or fp32 when F32),
-// each padded by 16 bytes; rows past M are zero.
+// each padded (kPadBf16 / kPadF32 bytes); rows past M are zero.
 template <bool F32>
 __device__ __forceinline__ void stage_tokens(const GemvArgs& a, int MB, uint8_t* xs, int row_bytes) {
   const int per_row = a.K / 8;  // 16-byte chunks of bf16
@@ -209,7 +215,7 @@ struct TensorCoreEngine {
 template <int MT, bool F32X>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_cuda_cores(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int row_bytes = a.K * (F32X ? 4 : 2) + 16;
+  const int row_bytes = a.K * (F32X ? 4 : 2) + (F32X ? kPadF32 : kPadBf16);
   uint8_t* xs = smem + kRingBytes;
   stage_tokens<F32X>(a, MT, xs, row_bytes);
   CudaCoreEngine<MT, F32X> eng{a, xs, row_bytes, (int)(threadIdx.x & 31)};
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_cuda_cores(GemvArgs a
 template <int TB>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_tensor_cores(GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int row_bytes = a.K * 2 + 16;
+  const int row_bytes = a.K * 2 + kPadBf16;
   uint8_t* xs = smem + kRingBytes;
   stage_tokens<false>(a, 8 * TB, xs, row_bytes);
   TensorCoreEngine<TB> eng{a, xs, row_bytes, (int)(threadIdx.x & 31)};
@@ -326,16 +332,16 @@ int moe_gemv(const void* packed, const void* x, float* y, int rows, int k, int M
   // ring + token rows + 2 mbarriers per warp; the CUDA cores take fp32
   // token rows when they fit, else bf16
   const size_t bars = (size_t)kGemvWarps * 16;
-  const size_t f32 = kRingBytes + (size_t)M * (4 * (size_t)k + 16) + bars;
+  const size_t f32 = kRingBytes + (size_t)M * (4 * (size_t)k + kPadF32) + bars;
   GemvKernel kern;
   size_t smem;
   if (engine == MOE_GEMV_CUDA_CORES) {
     const bool fits = f32 <= kSmemLimit;
     kern = fits ? cuda_core_kernel<true>(M) : cuda_core_kernel<false>(M);
-    smem = fits ? f32 : kRingBytes + (size_t)M * (2 * (size_t)k + 16) + bars;
+    smem = fits ? f32 : kRingBytes + (size_t)M * (2 * (size_t)k + kPadBf16) + bars;
   } else {
     kern = M <= 8 ? gemv_tensor_cores<1> : gemv_tensor_cores<2>;
-    smem = kRingBytes + (size_t)(M <= 8 ? 8 : 16) * (2 * (size_t)k + 16) + bars;
+    smem = kRingBytes + (size_t)(M <= 8 ? 8 : 16) * (2 * (size_t)k + kPadBf16) + bars;
   }
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) {
     fail("%s", cudaGetErrorString(e));
