@@ -62,7 +62,7 @@ typedef struct moe_layer moe_layer_t; /* opaque; owned by the library */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or handle     */
-  MOE_ERR_UNSUPPORTED = 2,    /* valid request outside what this build runs */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid request outside what the library supports */
   MOE_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed       */
   MOE_ERR_OOM = 4,            /* device allocation failed at create         */
   MOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded in-kernel wait gave up           */
