@@ -19,6 +19,9 @@ with a barrier and a device synchronize on both sides; max over ranks.
     python bench.py --sweep               # M x routing sweep (writes JSON lines)
     python bench.py --lm-head [--M 1]     # the bf16 vocabulary projection
     python bench.py --crossover           # the contraction on CUDA cores vs tensor cores, M_e = 1..16
+    torchrun ... bench.py --gpus N --tp   # the layer split N ways (tensor parallel): every rank streams
+                                          # 1/N of each expert, an all-gather of the fp32 partials and
+                                          # their ordered sum end each call
 """
 from __future__ import annotations
 
@@ -41,6 +44,7 @@ sys.path.insert(0, ROOT)
 METRIC = "cold-L2 µs/MoE-layer call and achieved HBM GB/s (% of GB300 peak) at M=1/6/16"
 UNIT = "µs/call"
 L2_BYTES = 126 * 1024 * 1024      # replaced by the device's value when a GPU is present
+NOMINAL_HBM_GBS = 8000.0          # the GB300's nominal HBM3e bandwidth (~8 TB/s)
 
 
 # --------------------------------------------------------------- helpers --
@@ -74,12 +78,22 @@ TRAFFIC_FILES = {False: os.path.join(ROOT, "profiles", "layer_traffic.json"),
 
 
 def measured_peaks():
+    """HBM copy bandwidth measured on the GB300s (MEASURED_PEAKS.json),
+    else the earlier measurement of 6.8 TB/s, with a warning on stderr."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
+    print("bench: MEASURED_PEAKS.json not found; fractions use the fallback peak of 6800 GB/s",
+          file=sys.stderr, flush=True)
     return 6800.0, "fallback"
+
+
+def fractions(gbs, peak):
+    """Achieved bandwidth as a fraction of the measured copy peak and of the
+    nominal ~8 TB/s."""
+    return {"frac_of_peak": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
 
 
 class ClockSampler:
@@ -200,8 +214,13 @@ class Workload:
             self.layers.append(MoELayer(w_r, w_gu, w_d, topk=shape.topk, **kw))
             del w_r, w_gu, w_d, kw
             torch.cuda.empty_cache()
+        self.n_use = len(self.layers)
         self.set_routing(zipf)
         self.new_pool(M, pool)
+
+    def use_layers(self, n):
+        """Cycle the first n layers (at most all of them)."""
+        self.n_use = max(1, min(n, len(self.layers)))
 
     def set_routing(self, zipf):
         from weight_streaming_expert_gb300 import workloads as wl
@@ -219,9 +238,12 @@ class Workload:
         self.outs = [torch.empty((M, H), dtype=torch.bfloat16, device=self.device) for _ in range(pool)]
         self.idxs = [torch.empty((M, k), dtype=torch.int32, device=self.device) for _ in range(pool)]
 
+    def layer(self, c):
+        return self.layers[c % self.n_use]
+
     def call(self, c, stream=None):
         i = c % len(self.xs)
-        self.layers[c % len(self.layers)](self.xs[i], out=self.outs[i], topk_idx=self.idxs[i], stream=stream)
+        self.layer(c)(self.xs[i], out=self.outs[i], topk_idx=self.idxs[i], stream=stream)
 
     def close(self):
         for layer in self.layers:
@@ -309,8 +331,7 @@ def time_kernel_alone(wkl, calls):
         with torch.cuda.graph(g, stream=s):
             for c in range(calls):
                 i = c % len(wkl.xs)
-                layer = wkl.layers[c % len(wkl.layers)]
-                layer.forward_timed(wkl.xs[i], wkl.outs[i], wkl.idxs[i], evs[c], stream=s)
+                wkl.layer(c).forward_timed(wkl.xs[i], wkl.outs[i], wkl.idxs[i], evs[c], stream=s)
     g.replay()
     torch.cuda.synchronize()
     g.replay()
@@ -328,18 +349,17 @@ def phase_breakdown(wkl, reps=2):
     import torch
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    n = reps * len(wkl.layers)
+    n = reps * wkl.n_use
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
             for c in range(n):
                 i = c % len(wkl.xs)
-                wkl.layers[c % len(wkl.layers)](wkl.xs[i], out=wkl.outs[i], topk_idx=wkl.idxs[i], stream=s,
-                                                 trace=True)
+                wkl.layer(c)(wkl.xs[i], out=wkl.outs[i], topk_idx=wkl.idxs[i], stream=s, trace=True)
     g.replay()
     torch.cuda.synchronize()
     rows = []
-    for layer in wkl.layers:
+    for layer in wkl.layers[:wkl.n_use]:
         t = layer.read_trace().astype(np.float64)
         t0 = t[:, 0].min()
         r = (t - t0) / 1000.0
@@ -368,7 +388,7 @@ def time_e2e(wkl, steps):
     def one(c):
         i = c % P
         dx[i].copy_(hx[i], non_blocking=True)
-        wkl.layers[c % len(wkl.layers)](dx[i], out=wkl.outs[i], topk_idx=wkl.idxs[i], stream=s)
+        wkl.layer(c)(dx[i], out=wkl.outs[i], topk_idx=wkl.idxs[i], stream=s)
         ho[i].copy_(wkl.outs[i], non_blocking=True)
         hi[i].copy_(wkl.idxs[i], non_blocking=True)
 
@@ -480,7 +500,13 @@ def run_ours(args):
     shape = wl.SHAPES[args.shape]
     M = args.M
     n_layers = n_layers_for(M, shape, l2, args.layers, args.fp8)
-    wkl = Workload(shape, n_layers, M, args.pool, args.zipf, dev, variant=args.variant, fp8=args.fp8)
+    # the side measurements (M = 1, M = 16 Zipf) cycle as many layers as
+    # their own per-call bytes need to keep L2 cold: build them all once
+    side = ((1, False), (16, True)) if (args.all_m and rank == 0) else ()
+    n_side = {m2: n_layers_for(m2, shape, l2, args.layers, args.fp8) for m2, _ in side}
+    wkl = Workload(shape, max([n_layers] + list(n_side.values())), M, args.pool, args.zipf, dev,
+                   variant=args.variant, fp8=args.fp8)
+    wkl.use_layers(n_layers)
     ms, active, clocks = time_graph(wkl, args.steps, args.warmup, pg, sample_clocks=(rank == 0),
                                     gpu_index=local)
     mean_active = float(np.mean(active)) + (1.0 if args.variant else 0.0)  # + the shared expert
@@ -507,19 +533,25 @@ def run_ours(args):
         e2e_us, h2d, d2h = time_e2e(wkl, min(args.steps, 4000))
         e2e_us = max_over_ranks(pg, e2e_us)
     by_m = {}
-    if args.all_m and rank == 0:
-        for m2, z2 in ((1, False), (16, True)):
-            wkl.set_routing(z2)
-            wkl.new_pool(m2, args.pool)
-            ms2, act2, _ = time_graph(wkl, min(args.steps, 4000), args.warmup, None)
-            act2 = [a + (1 if args.variant else 0) for a in act2]
-            b2 = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, m2, float(np.mean(act2)),
-                                   args.fp8)
-            by_m[f"M={m2}" + ("_zipf" if z2 else "")] = {
-                "us_per_call": round(ms2 * 1000, 3), "achieved_gbs": round(b2 / (ms2 * 1e-3) / 1e9, 1),
-                "frac_of_peak": round(b2 / (ms2 * 1e-3) / 1e9 / peak, 4),
-                "mean_active_experts": round(float(np.mean(act2)), 2)}
-        wkl.set_routing(args.zipf)
+    for m2, z2 in side:
+        wkl.set_routing(z2)
+        wkl.new_pool(m2, args.pool)
+        wkl.use_layers(n_side[m2])
+        by_m[f"M={m2}" + ("_zipf" if z2 else "")] = side_measurement(wkl, args, shape, m2, peak)
+    wkl.set_routing(args.zipf)
+    fp8_by_m = {}
+    if side and not args.fp8 and not args.variant and args.fp8_side:
+        # the same layer shape with fp8 (E4M3) expert weights: half the bytes
+        wkl.close()
+        torch.cuda.empty_cache()
+        n8 = {m2: n_layers_for(m2, shape, l2, args.layers, True) for m2 in (6, 1)}
+        w8 = Workload(shape, max(n8.values()), 6, args.pool, False, dev, fp8=True)
+        for m2 in (6, 1):
+            w8.new_pool(m2, args.pool)
+            w8.use_layers(n8[m2])
+            fp8_by_m[f"M={m2}"] = side_measurement(w8, args, shape, m2, peak, fp8=True)
+        w8.close()
+        torch.cuda.empty_cache()
     cpu = None
     if not args.no_cpu_baseline and rank == 0:
         wkl.close()
@@ -542,14 +574,15 @@ def run_ours(args):
                        "l2_policy": f"inputs larger than L2: {n_layers} distinct layer weight sets cycled, "
                                     f"fresh x per call; L2 {l2 // (1024 * 1024)} MiB",
                        "graph_calls": min(64, args.steps), "parallelism": f"replicas x{ws}"},
-            "achieved_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-            "peak_gbs": peak, "peak_kind": peak_kind,
+            "achieved_gbs": round(gbs, 1), **fractions(gbs, peak),
+            "peak_gbs": peak, "peak_kind": peak_kind, "nominal_peak_gbs": NOMINAL_HBM_GBS,
             "mean_active_experts": round(mean_active, 2), "algorithmic_bytes_per_call": int(bytes_call),
             "kernel_us": {"moe_layer_kernel_in_chain": round(us, 3), "moe_layer_kernel_alone": round(alone_us, 3),
                           "alone_timing": "graph replay, no PDL, events around each launch"},
             "phases_us": phases,
             "roofline": {"bound": "hbm", "kernel": "moe_layer_kernel", "achieved": round(gbs, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": traffic,
+                         "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                          "algorithmic_bytes_per_launch": int(bytes_call), "peak_kind": peak_kind,
                          "launch_duration": "timed-region mean per launch (one launch per call, PDL-chained)"},
             "cpu_baseline": cpu,
@@ -560,9 +593,23 @@ def run_ours(args):
         }
         if by_m:
             line["by_M"] = by_m
+        if fp8_by_m:
+            line["fp8_experts_by_M"] = fp8_by_m
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def side_measurement(wkl, args, shape, M, peak, fp8=False):
+    """One side configuration, timed like the headline (graph replay of
+    exactly min(steps, 4000) calls, cold L2)."""
+    ms2, act2, _ = time_graph(wkl, min(args.steps, 4000), args.warmup, None)
+    act2 = [a + (1 if args.variant else 0) for a in act2]
+    b2 = algorithmic_bytes(shape.hidden, shape.n_experts, shape.topk, shape.inter, M, float(np.mean(act2)), fp8)
+    gbs = b2 / (ms2 * 1e-3) / 1e9
+    return {"us_per_call": round(ms2 * 1000, 3), "achieved_gbs": round(gbs, 1), **fractions(gbs, peak),
+            "mean_active_experts": round(float(np.mean(act2)), 2), "layers_cycled": wkl.n_use,
+            "calls_timed": min(args.steps, 4000)}
 
 
 def run_reference(args):
@@ -595,6 +642,100 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def tp_exchange(part, pg, world):
+    """The exchange step of a tensor-parallel split: every rank's fp32
+    partial output [M, H] gathered side by side into [world, M, H], the same
+    on every rank (an all-gather; the ordered sum that follows makes it an
+    all-reduce whose order is fixed)."""
+    import torch
+    if pg is None or world == 1:
+        return part.unsqueeze(0)
+    M, H = part.shape
+    out = torch.empty((world * M, H), dtype=part.dtype, device=part.device)
+    pg.all_gather_into_tensor(out, part.contiguous())
+    return out.view(world, M, H)
+
+
+def run_tp(args):
+    """The Ling-shaped layer split over the ranks (the post's TP4 when run on
+    4 GPUs): rank r holds gate/up rows and down columns [r I/N, (r+1) I/N)
+    of every expert and routes every token.  One step = the layer call with
+    its unrounded fp32 output, the all-gather of the N partials (NCCL), and
+    their ordered sum with one bf16 rounding (moe_combine_partials).  Launched
+    call by call (no graph: the collective is enqueued by the host)."""
+    import torch
+    from weight_streaming_expert_gb300 import MoELayer, combine_partials, tp_slice
+    from weight_streaming_expert_gb300 import workloads as wl
+    rank, ws, local, pg = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    prop = torch.cuda.get_device_properties(dev)
+    l2 = getattr(prop, "L2_cache_size", L2_BYTES) or L2_BYTES
+    shape = wl.SHAPES["ling"]
+    M = args.M
+    if shape.inter % ws or shape.inter // ws not in (128, 256, 512):
+        raise SystemExit(f"--tp: inter {shape.inter} cannot be split {ws} ways")
+    sl = wl.LayerShape(hidden=shape.hidden, n_experts=shape.n_experts, topk=shape.topk, inter=shape.inter // ws)
+    n_layers = n_layers_for(M, sl, l2, args.layers)
+    layers = []
+    for l in range(n_layers):
+        w_r, w_gu, w_d = wl.layer_weights(shape, seed=1000 + l, device=dev)
+        gu, d = tp_slice(w_gu, w_d, rank, ws)
+        del w_gu, w_d
+        layers.append(MoELayer(w_r, gu, d, topk=shape.topk))
+        del w_r, gu, d
+        torch.cuda.empty_cache()
+    xs = [wl.tokens(M, shape.hidden, seed=1_000_000 + i, device=dev) for i in range(args.pool)]
+    parts = [torch.empty((M, shape.hidden), dtype=torch.float32, device=dev) for _ in range(2)]
+    outs = [torch.empty((M, shape.hidden), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    idxs = [torch.empty((M, shape.topk), dtype=torch.int32, device=dev) for _ in range(args.pool)]
+    s = torch.cuda.current_stream()
+
+    def step(c):
+        i = c % args.pool
+        layers[c % n_layers](xs[i], out=parts[c % 2], topk_idx=idxs[i], out_f32=True, stream=s)
+        combine_partials(tp_exchange(parts[c % 2], pg, ws), out=outs[c % 2], stream=s)
+
+    for c in range(args.warmup):
+        step(c)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for c in range(args.steps):
+        step(c)
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.steps)
+    active = [int(torch.unique(idxs[c % args.pool]).numel()) for c in range(min(args.steps, args.pool))]
+    status = max(layer.status() for layer in layers)
+    for layer in layers:
+        layer.close()
+    peak, peak_kind = measured_peaks()
+    per_gpu = algorithmic_bytes(sl.hidden, sl.n_experts, sl.topk, sl.inter, M, float(np.mean(active)))
+    us = ms * 1000.0
+    gbs = per_gpu / (us * 1e-6) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": False, "scaling": "strong",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,0.02) bf16 weights, N(0,1) bf16 tokens (random init, no checkpoint)",
+            "config": {"workload": f"Ling-shaped MoE step split {ws} ways (tensor parallel): hidden {shape.hidden}, "
+                                   f"{shape.n_experts} experts, top-{shape.topk}, inter {shape.inter} "
+                                   f"({sl.inter} per rank), M={M}, uniform routing",
+                       "M": M, "layers_cycled": n_layers, "x_pool": args.pool,
+                       "l2_policy": f"inputs larger than L2: {n_layers} distinct layer slices cycled, fresh x per call",
+                       "parallelism": f"tp{ws}", "exchange": "all-gather of fp32 partials + ordered sum, one rounding"},
+            "achieved_gbs_per_gpu": round(gbs, 1), **fractions(gbs, peak), "peak_kind": peak_kind,
+            "algorithmic_bytes_per_call_per_gpu": int(per_gpu), "mean_active_experts": round(float(np.mean(active)), 2),
+            "device_status": status, "gpu_launches": 2 * args.steps}), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def run_sweep(args):
     import torch
     from weight_streaming_expert_gb300 import workloads as wl
@@ -612,7 +753,7 @@ def run_sweep(args):
             gb = b / (ms * 1e-3) / 1e9
             print(json.dumps({"sweep": True, "M": M, "routing": "zipf" if zipf else "uniform",
                               "us_per_call": round(ms * 1000, 3), "achieved_gbs": round(gb, 1),
-                              "frac_of_peak": round(gb / peak, 4), "peak_kind": peak_kind,
+                              **fractions(gb, peak), "peak_kind": peak_kind,
                               "mean_active_experts": round(float(np.mean(active)), 2),
                               "phases_us": phase_breakdown(wkl, reps=1)}), flush=True)
     wkl.close()
@@ -797,6 +938,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all-m", dest="all_m", action="store_false",
                     help="skip the M=1 and M=16 (Zipf) side measurements")
+    ap.add_argument("--no-fp8-side", dest="fp8_side", action="store_false",
+                    help="skip the fp8-expert M=6 and M=1 side measurements")
+    ap.add_argument("--tp", action="store_true",
+                    help="split every layer over the ranks (tensor parallel): 1/N of each expert per rank, "
+                         "fp32 partial outputs all-gathered and summed in rank order")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle timing")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--fp8", action="store_true", help="layers with fp8 (E4M3) expert weights and row scales")
@@ -820,6 +966,8 @@ def main(argv=None):
         run_sweep(args)
     elif args.crossover:
         run_crossover(args)
+    elif args.tp:
+        run_tp(args)
     else:
         run_ours(args)
 

@@ -5,12 +5,17 @@
  *   router gate matvec -> softmax top-k with renormalisation -> on-device
  *   token->expert compaction -> fused gate/up GEMV + SwiGLU -> down GEMV with
  *   the routing-weighted combine in its epilogue.
- * One persistent kernel (one CTA per SM, grid-wide waits inside), chained
- * to the previous work on the stream with Programmatic Dependent Launch and
- * capturable in a CUDA graph.  No host synchronisation, no allocation and no
- * device->host copy happens inside the forward call.  The kernel needs the
- * whole GPU: every one of its CTAs must be resident at once (they are, one
- * per SM, when no other work holds an SM for the kernel's whole duration).
+ * One persistent kernel (one CTA per SM by default, grid-wide waits
+ * inside), chained to the previous work on the stream with Programmatic
+ * Dependent Launch and capturable in a CUDA graph.  No host
+ * synchronisation, no allocation and no device->host copy happens inside the
+ * forward call.  Every CTA of the kernel must be resident at once: they are
+ * when no other work holds an SM for the kernel's whole duration.  A caller
+ * that runs other kernels beside the layer (a collective on a second
+ * stream, say) gives the layer fewer CTAs with moe_set_grid and leaves the
+ * other SMs to that work; a kernel whose CTAs cannot all become resident
+ * reports MOE_ERR_DEVICE_TIMEOUT through moe_get_status (its waits are
+ * bounded), it never hangs.
  *
  * Source of the method (page title and section):
  *   "How Ling-3.0-flash reduces batch 1 decoding latency by 54% on 4
@@ -78,6 +83,16 @@ typedef enum {
                                and updated when the pointers change           */
 #define MOE_FWD_TRACE 0x4u  /* record per-CTA phase timestamps of this call
                                (read with moe_read_trace); same results       */
+#define MOE_FWD_OUT_F32 0x8u /* `out` is fp32 [M][H] and receives the combine's
+                                fp32 sums unrounded: the partial output of one
+                                slice of a tensor-parallel split (see
+                                moe_combine_partials)                          */
+#define MOE_FWD_TEST_SKIP_ARRIVAL 0x40000000u
+                            /* test aid: one CTA leaves out one grid-wide
+                               arrival, so the call's dependent waits run out
+                               after the handle's wait limit and
+                               moe_get_status reports MOE_ERR_DEVICE_TIMEOUT;
+                               the outputs of such a call are undefined        */
 
 /*
  * moe_create -- build a layer handle from bf16 weights.
@@ -191,7 +206,9 @@ int moe_forward(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx,
 /*
  * moe_forward_ex -- moe_forward with options.
  *   topk_w  NULL, or device fp32 [M][k] receiving the routing weights.
- *   flags   MOE_FWD_NO_PDL and/or MOE_FWD_GRAPH.
+ *   flags   MOE_FWD_NO_PDL, MOE_FWD_GRAPH, MOE_FWD_TRACE, MOE_FWD_OUT_F32
+ *           (then `out` is fp32 [M][H], 4-byte aligned: out[m] = the fp32
+ *           sum over slots before the final rounding).
  * Results are bitwise identical for every flag combination (PDL and graph
  * replay change scheduling only).  MOE_FWD_GRAPH on a stream that is being
  * captured by the caller falls back to plain launches (they join the
@@ -219,6 +236,50 @@ int moe_forward_timed(moe_layer_t* h, const void* x, void* out,
  *         (synchronously); the caller keeps ownership of `bias`.
  */
 int moe_set_router_bias(moe_layer_t* h, const float* bias);
+
+/*
+ * moe_set_grid -- the number of CTAs a forward call of this handle launches.
+ *   ctas  1 .. SMs of the device, or 0 for one per SM (the default).
+ * The layer kernel's CTAs wait on one another, so all of them must be
+ * resident at once; a caller that runs other kernels concurrently with the
+ * layer (for example a collective on another stream) leaves SMs to them by
+ * giving the layer fewer CTAs.  The work is split over gridDim, so results
+ * are the same for every grid (bit for bit).  Synchronises the device and
+ * restarts the handle's arrival counts (no forward call of the handle may be
+ * in flight); drops the handle's cached graphs.  MOE_ERR_UNSUPPORTED if the
+ * grid cannot be resident on an idle device, MOE_ERR_INVALID_ARG outside
+ * the range.  Graphs captured by the caller keep the grid they captured.
+ */
+int moe_set_grid(moe_layer_t* h, int ctas);
+
+/*
+ * moe_set_wait_limit -- limit (ns) of every bounded wait inside the layer
+ * kernel (0: the default, 2 s).  A forward call whose waits run out leaves
+ * its outputs undefined and is reported by moe_get_status.  Tests set a
+ * short limit to make a wait run out quickly; graphs cached by the handle
+ * are dropped (they hold the old limit).
+ */
+int moe_set_wait_limit(moe_layer_t* h, unsigned long long ns);
+
+/*
+ * moe_combine_partials -- the exchange step of a tensor-parallel split of
+ * the layer ("PDL: ..." section: the MoE chain ends in an all-reduce of the
+ * GPUs' partial outputs; the post splits the layer four ways).  Each GPU
+ * holds 1/G of every expert's intermediate rows (gate and up rows
+ * [r*I/G, (r+1)*I/G) and the matching down columns) and runs the full
+ * routing; its moe_forward_ex(..., MOE_FWD_OUT_F32) output is the fp32
+ * partial sum over its slice.  This call sums G such partials in order and
+ * rounds once to bf16, so the split layer rounds exactly once, like the
+ * unsplit one:
+ *   out[i] = bf16( ((parts[0][i] + parts[1][i]) + ...) + parts[G-1][i] ).
+ *   parts  device fp32 [n_parts][n] (contiguous, as an all-gather leaves
+ *          them), 16-byte aligned.
+ *   n      elements per part (M * hidden), a multiple of 4.
+ *   out    device bf16 [n], 8-byte aligned; must not overlap parts.
+ * Asynchronous on `stream`; allocates nothing.  MOE_ERR_INVALID_ARG for bad
+ * pointers, sizes or alignment; MOE_ERR_CUDA if the launch fails.
+ */
+int moe_combine_partials(const float* parts, int n_parts, size_t n, void* out, moe_stream_t stream);
 
 /*
  * moe_get_status -- synchronises the device, then returns and clears the
@@ -257,6 +318,8 @@ typedef struct {
   float routed_scale;      /* factor on every routed weight */
   int bias_selection_only; /* 1 if the router bias only picks the experts */
   int fp8_experts;         /* 1 if the expert weights are E4M3 codes */
+  int grid_ctas;           /* CTAs a forward call launches (moe_set_grid) */
+  unsigned long long wait_limit_ns; /* limit of the kernel's bounded waits */
 } moe_info_t;
 
 int moe_get_info(const moe_layer_t* h, moe_info_t* out);
@@ -316,7 +379,10 @@ int moe_read_trace(moe_layer_t* h, uint64_t* out, int cap);
  * is one fixed array inside the library image, 78,080 bytes, which every GPU
  * that loads the library holds until the process exits.  Its arithmetic is
  * moe_forward's own router (same matvec split and summation order, same
- * top-k), so both give the same routing for the same x.
+ * top-k), so both give the same routing for the same x -- for a layer whose
+ * router bias shifts the logits for both the choice and the weights (the
+ * default; a layer made with bias_selection_only weighs its experts with the
+ * unbiased logits, this call with the biased ones).
  *   hidden, n_experts, topk   as for moe_create.
  *   x          device bf16 [M][hidden], 16-byte aligned.
  *   w_router   device bf16 [n_experts][hidden], 16-byte aligned; read in
@@ -333,13 +399,30 @@ int moe_read_trace(moe_layer_t* h, uint64_t* out, int cap);
  * the last call's contents (the counter that must start at zero is cleared by
  * each call on its stream), so calls whose work can overlap on the GPU --
  * different streams without ordering -- race.  Returns MOE_ERR_UNSUPPORTED
- * (with a moe_last_error() message) for M > 16 or sizes outside the limits,
- * MOE_ERR_INVALID_ARG for bad pointers, MOE_ERR_CUDA if set-up or the launch
- * fails.
+ * (with a moe_last_error() message) for M > 16, sizes outside the limits, or
+ * a device whose SM count gives moe_forward's matvec split more partial
+ * logits than the array holds (never on a 152-SM GB300: the split would
+ * differ, and with it the summation order); MOE_ERR_INVALID_ARG for bad
+ * pointers, MOE_ERR_CUDA if set-up or the launch fails.  Errors found on the
+ * device (a top-k without a candidate, which cannot happen while
+ * topk <= n_experts) are not returned here: read them with
+ * moe_route_static_read_status before the next call on the device.
  */
 int moe_route_static(int hidden, int n_experts, int topk, const void* x,
                      const void* w_router, const float* bias, int M,
                      int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/*
+ * moe_route_static_read_status -- copy the device status word of the last
+ * moe_route_static call on the current device to `status` (device or host
+ * int, 4-byte aligned) with one asynchronous copy on `stream`; allocates
+ * nothing.  The value is 0, or 8 if a top-k found no candidate.  Enqueue it
+ * on the stream of the call it reads, before the next moe_route_static call
+ * (which clears the word); read `status` after the stream reaches the copy.
+ * MOE_ERR_INVALID_ARG for a NULL pointer, MOE_ERR_CUDA if set-up or the copy
+ * fails.
+ */
+int moe_route_static_read_status(int* status, moe_stream_t stream);
 
 /* moe_destroy -- synchronises the handle's device, frees everything.
  * NULL is a no-op. */

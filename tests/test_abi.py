@@ -129,3 +129,34 @@ def test_gemv_zero_tokens_and_pack_checks(L):
     assert L.moe_gemv_pack(ctypes.c_void_p(24), ctypes.c_void_p(32), 16, 64, None) == native.MOE_ERR_INVALID_ARG
     assert "aligned" in native.last_error()
     assert L.moe_gemv_pack(ctypes.c_void_p(16), ctypes.c_void_p(32), 15, 64, None) == native.MOE_ERR_INVALID_ARG
+
+
+def test_new_entry_points_reject_bad_arguments_before_the_gpu(L):
+    p = ctypes.c_void_p
+    assert L.moe_set_grid(None, 0) == native.MOE_ERR_INVALID_ARG
+    assert L.moe_set_wait_limit(None, 0) == native.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_partials(None, 2, 16, None, None) == native.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_partials(p(16), 2, 18, p(4096), None) == native.MOE_ERR_INVALID_ARG   # n % 4
+    assert L.moe_combine_partials(p(16), 0, 16, p(4096), None) == native.MOE_ERR_INVALID_ARG   # no parts
+    assert L.moe_combine_partials(p(20), 2, 16, p(4096), None) == native.MOE_ERR_INVALID_ARG   # misaligned
+    assert "aligned" in native.last_error()
+    assert L.moe_combine_partials(p(16), 2, 16, p(32), None) == native.MOE_ERR_INVALID_ARG     # overlap
+    assert "overlaps" in native.last_error()
+    assert L.moe_combine_partials(p(16), 2, 0, p(4096), None) == native.MOE_OK                 # nothing to do
+    assert L.moe_route_static_read_status(None, None) == native.MOE_ERR_INVALID_ARG
+    assert L.moe_route_static_read_status(p(2), None) == native.MOE_ERR_INVALID_ARG            # misaligned
+
+
+def test_info_struct_matches_the_header():
+    """moe_info_t's fields, in order, as the header declares them."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    end = src.index("} moe_info_t;")
+    body = src[src.rindex("typedef struct {", 0, end) + len("typedef struct {"):end]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            names += [n.strip() for n in decl.split(None, 1)[1].split(",")] if not decl.startswith("unsigned long long") \
+                else [n.strip() for n in decl[len("unsigned long long"):].split(",")]
+    assert names == [f for f, _ in native.moe_info_t._fields_]

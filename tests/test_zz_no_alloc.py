@@ -10,6 +10,7 @@ failure has already run every other test.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
@@ -60,6 +61,57 @@ def test_static_routing_equals_layer_routing_on_consecutive_calls():
     layer.close()
 
 
+_W = {}
+
+
+def _router(E, H=2560):
+    """One router weight per expert count, kept for the module."""
+    if E not in _W:
+        g = torch.Generator().manual_seed(1234 + E)
+        _W[E] = (torch.randn((E, H), generator=g) * wl.WEIGHT_STD).to(torch.bfloat16)
+    return _W[E]
+
+
+@pytest.mark.parametrize("E", [17, 512, 1000])
+@pytest.mark.parametrize("k", [1, 8, 32])
+@pytest.mark.parametrize("M", [1, 6, 16])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_static_routing_matches_the_oracle(oracle, E, k, M, with_bias):
+    """Expert ids bit-exact against the oracle's router and top-k (up to the
+    documented near-ties), weights within a few fp32 ulps, and a clean status
+    word read back through moe_route_static_read_status."""
+    if k > E:
+        pytest.skip("k > E is refused")
+    from tests import parity
+    H = 2560
+    w = _router(E, H)
+    x = wl.tokens(M, H, seed=70 + M + E)
+    bias = None
+    if with_bias:
+        bias = torch.from_numpy((np.random.default_rng(E + k).standard_normal(E) * 0.5).astype(np.float32))
+    route = _route_static()
+    wd, xd = w.to(DEV), x.to(DEV)
+    bd = None if bias is None else bias.to(DEV)
+    idx = torch.full((M, k), -1, dtype=torch.int32, device=DEV)
+    tw = torch.full((M, k), -1.0, dtype=torch.float32, device=DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    rc = route(H, E, k, _p(xd), _p(wd), _p(bd), M, _p(idx), _p(tw), sp)
+    assert rc == native.MOE_OK, native.last_error()
+    assert native.lib().moe_route_static_read_status(_p(status), sp) == native.MOE_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    logits = oracle.router_logits(wl.bf16_bits(x), wl.bf16_bits(w), None if bias is None else bias.numpy())
+    ref_idx, ref_w = oracle.topk_softmax(logits, k)
+    gi, gw = idx.cpu().numpy(), tw.cpu().numpy()
+    for m in range(M):
+        assert parity.routing_ok(gi[m], ref_idx[m], logits[m]), f"token {m}: {gi[m]} vs {ref_idx[m]}"
+        want = ref_w[m] if np.array_equal(gi[m], ref_idx[m]) else oracle.weights_for_set(logits[m], gi[m])
+        np.testing.assert_allclose(gw[m], want, rtol=2e-6, atol=1e-7)
+        assert abs(float(gw[m].sum()) - 1.0) <= 1e-5
+
+
 def test_static_routing_rejects_sizes_beyond_its_scratch():
     route = _route_static()
     x = torch.zeros((17, 256), dtype=torch.bfloat16, device=DEV)
@@ -70,3 +122,4 @@ def test_static_routing_rejects_sizes_beyond_its_scratch():
     assert "16 tokens" in native.last_error()
     rc = route(256, 2048, 2, _p(x), _p(w), None, 1, _p(idx), None, None)
     assert rc == native.MOE_ERR_UNSUPPORTED
+    assert native.lib().moe_route_static_read_status(None, None) == native.MOE_ERR_INVALID_ARG

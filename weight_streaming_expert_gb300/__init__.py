@@ -7,14 +7,11 @@ vocabulary projection of the same decode step (``include/lm_head.h``).  Importin
 loads nothing; the CUDA library is loaded (and must exist) on first use.
 """
 
-__all__ = ["MoELayer", "LmHead"]
+__all__ = ["MoELayer", "LmHead", "tp_slice", "combine_partials"]
 
 
 def __getattr__(name):
-    if name == "MoELayer":
-        from .layer import MoELayer
-        return MoELayer
-    if name == "LmHead":
-        from .layer import LmHead
-        return LmHead
+    if name in __all__:
+        from . import layer
+        return getattr(layer, name)
     raise AttributeError(name)

@@ -46,8 +46,9 @@ enum : int {
   kSyncWords = 224,
 };
 
-// A bounded wait gives up after this long (the kernels run for microseconds;
-// reaching it means a bug, never a slow call).
+// A bounded wait gives up after this long by default (the kernels run for
+// microseconds; reaching it means a bug or an SM held by other work, never a
+// slow call).  A layer handle can set a shorter limit for its own kernel.
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 // Bits of the sticky device status word.
@@ -129,10 +130,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false after the
-// timeout (the caller records an error bit and leaves its loop).
+// Wait for the phase with the given parity to complete; false after `limit`
+// ns (the caller records an error bit and leaves its loop).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          unsigned long long* waited = nullptr) {
+                                          unsigned long long* waited = nullptr,
+                                          unsigned long long limit = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
@@ -140,7 +142,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long dt = global_timer_ns() - t0;
-    if (dt > kWaitTimeoutNs) {
+    if (dt > limit) {
       if (waited) *waited = dt;
       return false;
     }
@@ -150,8 +152,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 // Warp-uniform bounded wait: every lane waits and the lanes agree on the
 // outcome by vote, so a timeout never splits the warp before a .aligned
 // instruction (mma.sync) or a __syncwarp().
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned long long* waited) {
-  const bool ok = mbar_wait(bar, parity, waited);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned long long* waited,
+                                          unsigned long long limit = kWaitTimeoutNs) {
+  const bool ok = mbar_wait(bar, parity, waited, limit);
   return __all_sync(0xffffffffu, ok);
 }
 

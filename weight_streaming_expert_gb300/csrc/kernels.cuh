@@ -17,7 +17,8 @@ struct LayerArgs {
   const uint8_t* w_down;          // packed down tiles, see pack.cu
   const float* s_gu;              // fp8 experts: [E][2I] gate/up row scales (else unused)
   const float* s_d;               // fp8 experts: [E][H] down row scales (else unused)
-  __nv_bfloat16* out;             // [M][H]
+  __nv_bfloat16* out;             // [M][H] (unused when out_f32 is set)
+  float* out_f32;                 // nullptr, or [M][H]: the combine's fp32 sums, not rounded
   int32_t* topk_idx;              // [M][K] caller output
   float* topk_w;                  // [M][K] caller output or nullptr
   int M, H, E, K, I;
@@ -32,8 +33,15 @@ struct LayerArgs {
   int shared;                     // 1: expert E is a shared expert every token passes (weight 1)
   float routed_scale;             // factor on every routed weight
   int sel_only;                   // 1: the bias picks the experts, unbiased logits weigh them
+  unsigned long long wait_ns;     // limit of every bounded wait (ns)
+  int test_flags;                 // kTestSkipArrival: see below
   Workspace ws;
 };
+
+// Test aid: CTA 0 leaves out its arrival at the grid-wide count of reduced
+// static gate/up tiles, so every CTA's wait on that count runs out (bounded)
+// and the call reports MOE_ERR_DEVICE_TIMEOUT through moe_get_status.
+constexpr int kTestSkipArrival = 1;
 
 // The layer kernel: grid = #SMs x kExpertThreads, dynamic shared memory
 // layer_smem_bytes(ring_bytes, NP, buckets).  KPW = H/256.

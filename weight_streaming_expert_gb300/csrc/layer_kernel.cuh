@@ -139,7 +139,7 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
 
 // Bounded acquire-spin until the count at `word` reaches `target`.
 __device__ inline bool grid_wait(const Workspace& ws, const unsigned* word, unsigned long long target,
-                                 int phase) {
+                                 int phase, unsigned long long limit) {
   const unsigned long long* cnt = reinterpret_cast<const unsigned long long*>(word);
   if (ld_acquire64(cnt) >= target) return true;
   const unsigned long long t0 = global_timer_ns();
@@ -147,7 +147,7 @@ __device__ inline bool grid_wait(const Workspace& ws, const unsigned* word, unsi
     __nanosleep(32);
     if (ld_acquire64(cnt) >= target) return true;
     const unsigned long long dt = global_timer_ns() - t0;
-    if (dt > kWaitTimeoutNs) {
+    if (dt > limit) {
       record_timeout(ws, phase, kErrTimeoutGrid, (int)(target % gridDim.x), 0, 0, dt);
       return false;
     }
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
 
   // ---- 3. top-k of every token, compaction (every CTA, shared memory only)
   for (int m = warp; m < a.M; m += kExpertThreads / 32) {
-    const float w = topk_dispatch(PolledPlanes{part + (size_t)m * a.E, plane}, a.ks, a.bias, a.E, a.K, lane,
+    const float w = topk_dispatch(PolledPlanes{part + (size_t)m * a.E, plane, a.wait_ns}, a.ks, a.bias, a.E, a.K, lane,
                                   a.ws.status, rt.s_e + m * a.K, VARIANT && a.sel_only != 0);
     __syncwarp();
     if (lane < a.K) {
@@ -365,22 +365,22 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     unsigned long long waited = 0;
     const unsigned long long target = *call_idx * gridDim.x;
     // static gate/up tiles reduced here -> counted; every CTA counted -> level 1
-    if (!mbar_wait(static_bar, 0, &waited)) {
+    if (!mbar_wait(static_bar, 0, &waited, a.wait_ns)) {
       record_timeout(a.ws, 2, kErrTimeoutReduce, -3, 0, static_bar, waited);
       return;
     }
-    grid_count(a.ws.sync + kSyncStaticDone);
+    if (!(a.test_flags & kTestSkipArrival) || blockIdx.x != 0) grid_count(a.ws.sync + kSyncStaticDone);
     stamp(a, 18);
-    if (!grid_wait(a.ws, a.ws.sync + kSyncStaticDone, target, 2)) return;
+    if (!grid_wait(a.ws, a.ws.sync + kSyncStaticDone, target, 2, a.wait_ns)) return;
     mbar_arrive(level1);
     stamp(a, 6);
     // all gate/up tiles reduced here -> counted; every CTA counted -> level 2
-    if (!mbar_wait(done, 0, &waited)) {
+    if (!mbar_wait(done, 0, &waited, a.wait_ns)) {
       record_timeout(a.ws, 2, kErrTimeoutReduce, -4, 0, done, waited);
       return;
     }
     grid_count(a.ws.sync + kSyncGateUpDone);
-    if (!grid_wait(a.ws, a.ws.sync + kSyncGateUpDone, target, 2)) return;
+    if (!grid_wait(a.ws, a.ws.sync + kSyncGateUpDone, target, 2, a.wait_ns)) return;
     mbar_arrive(level2);
     stamp(a, 17);
     return;
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       }
       if (tile >= T_gu) break;
       const int s = j % S;
-      if (j >= S && !mbar_wait(empty(s), ((j / S) - 1) & 1, &waited)) {
+      if (j >= S && !mbar_wait(empty(s), ((j / S) - 1) & 1, &waited, a.wait_ns)) {
         record_timeout(a.ws, 2, kErrTimeoutEmpty, j, S, empty(s), waited);
         ok = false;
         break;
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int n_gu = j;
     if (ok) {  // end marker for the consumers
       const int s = j % S;
-      if (j >= S && !mbar_wait(empty(s), ((j / S) - 1) & 1, &waited)) {
+      if (j >= S && !mbar_wait(empty(s), ((j / S) - 1) & 1, &waited, a.wait_ns)) {
         record_timeout(a.ws, 2, kErrTimeoutEmpty, j, S, empty(s), waited);
         ok = false;
       } else {
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     auto ensure_ready = [&](int g) -> bool {
       const int need = g < g_static ? 1 : 2;
       if (level >= need) return true;
-      if (!mbar_wait(need == 1 ? level1 : level2, 0, &waited)) {
+      if (!mbar_wait(need == 1 ? level1 : level2, 0, &waited, a.wait_ns)) {
         record_timeout(a.ws, 3, kErrTimeoutReduce, -5 - need, SD, need == 1 ? level1 : level2, waited);
         return false;
       }
@@ -479,13 +479,13 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         const int jf = n_gu - S + r_done;
         if (jf < 0) continue;  // a stage this CTA never used
         const int st = jf % S;
-        if (!mbar_wait(empty(st), (jf / S) & 1, &waited)) {
+        if (!mbar_wait(empty(st), (jf / S) & 1, &waited, a.wait_ns)) {
           record_timeout(a.ws, 3, kErrTimeoutEmpty, jf, S, empty(st), waited);
           return false;
         }
       }
       if (rank >= S && !red_free) {
-        if (!mbar_wait(done, 0, &waited)) {
+        if (!mbar_wait(done, 0, &waited, a.wait_ns)) {
           record_timeout(a.ws, 3, kErrTimeoutEmpty, -1, S, done, waited);
           return false;
         }
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
           ok = false;
           break;
         }
-      } else if (!mbar_wait(dempty(s), ((j2 / SD) - 1) & 1, &waited)) {
+      } else if (!mbar_wait(dempty(s), ((j2 / SD) - 1) & 1, &waited, a.wait_ns)) {
         record_timeout(a.ws, 3, kErrTimeoutEmpty, j2, SD, dempty(s), waited);
         ok = false;
         break;
@@ -543,6 +543,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         }
       }
       if (!ensure_ready(g)) {
+        // the copy just issued lands in a slot no consumer will read: wait
+        // for it (bounded) so that no copy is in flight when the CTA exits
+        if (!mbar_wait(dfull(s), (uint32_t)(j2 / SD) & 1u, &waited, a.wait_ns))
+          record_timeout(a.ws, 3, kErrTimeoutFull, j2, SD, dfull(s), waited);
         ok = false;
         break;
       }
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     if (a.trace) a.ws.trace[(size_t)blockIdx.x * kTraceSlots + 16] = (unsigned long long)j2;
     if (ok) {  // end marker (a first use needs no free bytes: only the id is written)
       const int s = j2 % SD;
-      if (j2 >= SD && !mbar_wait(dempty(s), ((j2 / SD) - 1) & 1, &waited)) {
+      if (j2 >= SD && !mbar_wait(dempty(s), ((j2 / SD) - 1) & 1, &waited, a.wait_ns)) {
         record_timeout(a.ws, 3, kErrTimeoutEmpty, j2, SD, dempty(s), waited);
       } else {
         dstage_tile[s] = -1;
@@ -579,7 +583,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     for (int j = 0;; ++j) {
       const int s = j % S;
       const uint32_t ph = (uint32_t)(j / S) & 1u;
-      if (!warp_wait(ready(s), ph, &waited)) {
+      if (!warp_wait(ready(s), ph, &waited, a.wait_ns)) {
         record_timeout(a.ws, 2, kErrTimeoutFull, j, S, ready(s), waited);
         break;
       }
@@ -623,7 +627,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
           }
         }
       }
-      if (!warp_wait(full(s), ph, &waited)) {
+      if (!warp_wait(full(s), ph, &waited, a.wait_ns)) {
         record_timeout(a.ws, 2, kErrTimeoutFull, j, S, full(s), waited);
         break;
       }
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       __syncwarp();
       if (lane == 0) mbar_arrive(redbar(slot));
       if (warp == slot) {  // this tile's reducer (rotates over the warps)
-        if (!warp_wait(redbar(slot), (uint32_t)(j >> 3) & 1u, &waited)) {
+        if (!warp_wait(redbar(slot), (uint32_t)(j >> 3) & 1u, &waited, a.wait_ns)) {
           record_timeout(a.ws, 2, kErrTimeoutReduce, j, S, redbar(slot), waited);
           break;
         }
@@ -747,7 +751,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     for (int j = 0;; ++j) {
       const int s = j % SD;
       const uint32_t ph = (uint32_t)(j / SD) & 1u;
-      if (!warp_wait(dready(s), ph, &waited)) {
+      if (!warp_wait(dready(s), ph, &waited, a.wait_ns)) {
         record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dready(s), waited);
         break;
       }
@@ -806,7 +810,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       auto consume_cell = [&](auto ns) -> bool {
         const int NS = ns;
         float4 rs = row_scales(cl * NS);  // the first slab's, while the data lands
-        if (!warp_wait(dfull(s), ph, &waited)) {
+        if (!warp_wait(dfull(s), ph, &waited, a.wait_ns)) {
           record_timeout(a.ws, 3, kErrTimeoutFull, j, SD, dfull(s), waited);
           return false;
         }
@@ -915,7 +919,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   consumers_sync();
   if (tid == 0) {
     grid_count(a.ws.sync + kSyncCount);
-    if (owner) grid_wait(a.ws, a.ws.sync + kSyncCount, *call_idx * gridDim.x, 3);
+    if (owner) grid_wait(a.ws, a.ws.sync + kSyncCount, *call_idx * gridDim.x, 3, a.wait_ns);
   }
   if (!owner) return;
   consumers_sync();
@@ -940,7 +944,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         if (k0 + i < a.K) sum += v[i];
     }
     if (shared) sum += vs;  // the shared slot, last
-    a.out[(size_t)m * a.H + r] = __float2bfloat16_rn(sum);
+    if (a.out_f32)
+      a.out_f32[(size_t)m * a.H + r] = sum;  // a partial of a split layer: rounded after the sum of the parts
+    else
+      a.out[(size_t)m * a.H + r] = __float2bfloat16_rn(sum);
   }
   if (tid == 0) stamp(a, 8);
 }

@@ -88,6 +88,8 @@ struct moe_layer {
   int kp() const { return K + shared; }  // pairs per token
   int ea() const { return E + shared; }  // packed experts
   int dev = 0, n_sms = 0;
+  int grid = 0;             // CTAs of a layer launch (all SMs unless moe_set_grid chose fewer)
+  unsigned long long wait_ns = kWaitTimeoutNs;  // limit of the kernel's bounded waits
   __nv_bfloat16* w_router = nullptr;
   uint8_t* w_gu = nullptr;  // packed gate/up tiles
   uint8_t* w_d = nullptr;   // packed down tiles
@@ -135,10 +137,17 @@ int cuda_fail(cudaError_t e, const char* what) {
   return MOE_ERR_CUDA;
 }
 
+// Arrival counts from zero, every partial logit of both buffers unwritten
+// (the state moe_create leaves).  Only while no kernel of the handle runs.
+void restart_counts(moe_layer* h) {
+  cudaMemset(h->ws.sync, 0, kSyncWords * 4);
+  cudaMemset(h->ws.part, 0xff, 2 * (size_t)h->ks * kMaxTokens * h->E * 4);
+}
+
 // Enqueue the layer kernel.  ev (2 events) brackets it for profiling; the
 // records are external event nodes when the stream is being captured.
 int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw, int M,
-                 cudaStream_t st, bool pdl, bool trace, cudaEvent_t* ev) {
+                 cudaStream_t st, bool pdl, bool trace, cudaEvent_t* ev, unsigned flags = 0u) {
   const LayerPlan& pl = h->plan_for(M);
   LayerArgs la{};
   la.x = static_cast<const __nv_bfloat16*>(x);
@@ -148,7 +157,9 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   la.w_down = h->w_d;
   la.s_gu = h->sc_gu;
   la.s_d = h->sc_d;
-  la.out = static_cast<__nv_bfloat16*>(out);
+  const bool f32 = (flags & MOE_FWD_OUT_F32) != 0;
+  la.out = f32 ? nullptr : static_cast<__nv_bfloat16*>(out);
+  la.out_f32 = f32 ? static_cast<float*>(out) : nullptr;
   la.topk_idx = idx;
   la.topk_w = tw;
   la.M = M; la.H = h->H; la.E = h->E; la.K = h->K; la.I = h->I;
@@ -163,6 +174,8 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   la.shared = h->shared;
   la.routed_scale = h->routed_scale;
   la.sel_only = h->sel_only;
+  la.wait_ns = h->wait_ns;
+  la.test_flags = (flags & MOE_FWD_TEST_SKIP_ARRIVAL) ? kTestSkipArrival : 0;
   la.ws = h->ws;
 
   cudaLaunchAttribute attr[1];
@@ -172,7 +185,7 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   c.stream = st;
   c.attrs = pdl ? attr : nullptr;
   c.numAttrs = pdl ? 1 : 0;
-  c.gridDim = dim3(h->n_sms);
+  c.gridDim = dim3(h->grid);
   c.blockDim = dim3(kExpertThreads);
   c.dynamicSmemBytes = layer_smem_bytes(pl.ring_bytes, M * h->kp(), h->ea());
 
@@ -189,15 +202,17 @@ int launch_layer(moe_layer* h, const void* x, void* out, int32_t* idx, float* tw
   return MOE_OK;
 }
 
-int check_forward_args(moe_layer* h, const void* x, const void* out, const int32_t* idx, int M) {
+int check_forward_args(moe_layer* h, const void* x, const void* out, const int32_t* idx, int M,
+                       unsigned flags = 0u) {
   if (!h) { set_err("null handle"); return MOE_ERR_INVALID_ARG; }
   if (M < 0) { set_err("M = %d < 0", M); return MOE_ERR_INVALID_ARG; }
   if (M > MOE_MAX_TOKENS) { set_err("M = %d exceeds %d", M, MOE_MAX_TOKENS); return MOE_ERR_UNSUPPORTED; }
   if (M == 0) return MOE_OK;
   if (!x || !out || !idx) { set_err("null x/out/topk_idx"); return MOE_ERR_INVALID_ARG; }
   if (!aligned16(x)) { set_err("x must be 16-byte aligned"); return MOE_ERR_INVALID_ARG; }
-  if ((reinterpret_cast<uintptr_t>(out) & 1u) || (reinterpret_cast<uintptr_t>(idx) & 3u)) {
-    set_err("out must be 2-byte and topk_idx 4-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(out) & ((flags & MOE_FWD_OUT_F32) ? 3u : 1u)) ||
+      (reinterpret_cast<uintptr_t>(idx) & 3u)) {
+    set_err("out must be 2-byte (fp32 out: 4-byte) and topk_idx 4-byte aligned");
     return MOE_ERR_INVALID_ARG;
   }
   return MOE_OK;
@@ -286,6 +301,7 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   h->fp8 = fp8 ? 1 : 0;
   h->dev = dev;
   h->n_sms = prop.multiProcessorCount;
+  h->grid = h->n_sms;
   h->tile_gu = (uint32_t)(kGateUpTileRows * hidden * 2);
   h->ks = gemv_split(hidden, n_experts, h->n_sms);
 
@@ -460,7 +476,7 @@ moe_layer_t* moe_create_fp8(int hidden, int n_experts, int topk, int inter, cons
 
 int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, float* topk_w, int M,
                    moe_stream_t stream, unsigned flags) {
-  int rc = check_forward_args(h, x, out, topk_idx, M);
+  int rc = check_forward_args(h, x, out, topk_idx, M, flags);
   if (rc != MOE_OK || M == 0) return rc;
   if (topk_w && (reinterpret_cast<uintptr_t>(topk_w) & 3u)) {
     set_err("topk_w must be 4-byte aligned");
@@ -480,7 +496,7 @@ int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, 
         cudaGraph_t g = nullptr;
         if ((e = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
           return cuda_fail(e, "begin capture");
-        rc = launch_layer(h, x, out, topk_idx, topk_w, M, h->cap_stream, pdl, trace, nullptr);
+        rc = launch_layer(h, x, out, topk_idx, topk_w, M, h->cap_stream, pdl, trace, nullptr, flags);
         e = cudaStreamEndCapture(h->cap_stream, &g);
         if (rc != MOE_OK) { if (g) cudaGraphDestroy(g); return rc; }
         if (e != cudaSuccess) return cuda_fail(e, "end capture");
@@ -503,7 +519,7 @@ int moe_forward_ex(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, 
       return MOE_OK;
     }
   }
-  return launch_layer(h, x, out, topk_idx, topk_w, M, st, pdl, trace, nullptr);
+  return launch_layer(h, x, out, topk_idx, topk_w, M, st, pdl, trace, nullptr, flags);
 }
 
 int moe_forward(moe_layer_t* h, const void* x, void* out, int32_t* topk_idx, int M, moe_stream_t stream) {
@@ -543,6 +559,49 @@ int moe_set_router_bias(moe_layer_t* h, const float* bias) {
   return MOE_OK;
 }
 
+int moe_set_wait_limit(moe_layer_t* h, unsigned long long ns) {
+  if (!h) { set_err("null handle"); return MOE_ERR_INVALID_ARG; }
+  h->wait_ns = ns ? ns : kWaitTimeoutNs;
+  drop_graphs(h);  // captured launches hold the old limit
+  return MOE_OK;
+}
+
+int moe_set_grid(moe_layer_t* h, int ctas) {
+  if (!h) { set_err("null handle"); return MOE_ERR_INVALID_ARG; }
+  if (ctas < 0 || ctas > h->n_sms) {
+    set_err("ctas = %d outside [0, %d] (0: one CTA per SM)", ctas, h->n_sms);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int g = ctas ? ctas : h->n_sms;
+  cudaError_t e;
+  int cur = 0;
+  if ((e = cudaGetDevice(&cur)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if ((e = cudaSetDevice(h->dev)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  // every CTA of the grid must be resident at once: one per SM on an idle
+  // device (the instances' occupancy at their largest shared-memory size)
+  for (int i = 0; i < 2; ++i) {
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->plan[i].kernel, kExpertThreads,
+                                                      h->plan[i].smem_max);
+    if (e != cudaSuccess || per_sm < 1 || (long long)per_sm * h->n_sms < g) {
+      cudaSetDevice(cur);
+      if (e != cudaSuccess) return cuda_fail(e, "occupancy");
+      set_err("a grid of %d CTAs cannot be resident at once (%d per SM x %d SMs)", g, per_sm, h->n_sms);
+      return MOE_ERR_UNSUPPORTED;
+    }
+  }
+  // the call index comes from the arrival count divided by the grid: start
+  // the counts again for the new grid (no kernel of this handle runs now)
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) { cudaSetDevice(cur); return cuda_fail(e, "synchronize"); }
+  h->grid = g;
+  restart_counts(h);
+  drop_graphs(h);
+  e = cudaDeviceSynchronize();
+  cudaSetDevice(cur);
+  if (e != cudaSuccess) return cuda_fail(e, "counter reset");
+  return MOE_OK;
+}
+
 int moe_get_status(moe_layer_t* h) {
   if (!h) { set_err("null handle"); return MOE_ERR_INVALID_ARG; }
   cudaError_t e;
@@ -558,8 +617,7 @@ int moe_get_status(moe_layer_t* h) {
     // a wait that gave up may have left the arrival counts between two
     // multiples of the grid: start them again from zero (no kernel runs
     // now), with every partial logit of both buffers unwritten again
-    cudaMemset(h->ws.sync, 0, kSyncWords * 4);
-    cudaMemset(h->ws.part, 0xff, 2 * (size_t)h->ks * kMaxTokens * h->E * 4);
+    restart_counts(h);
     set_err("device status bits 0x%x (1 stage wait, 2 free-stage wait, 4 reduction wait, 8 no top-k "
             "candidate, 16 grid-wide wait); first timeout: phase %llu kind %llu cta %llu stages %llu "
             "index %llu waited %llu ns barrier 0x%016llx thread %llu grid %llu",
@@ -577,6 +635,8 @@ int moe_get_info(const moe_layer_t* h, moe_info_t* o) {
   o->hidden = h->H; o->n_experts = h->E; o->topk = h->K; o->inter = h->I;
   o->max_tokens = MOE_MAX_TOKENS;
   o->n_sms = h->n_sms;
+  o->grid_ctas = h->grid;
+  o->wait_limit_ns = h->wait_ns;
   o->gateup_stages = h->plan[0].s_gu;
   o->down_stages = h->plan[0].s_d;
   o->gateup_tile_bytes = (int)h->tile_gu;

@@ -153,13 +153,12 @@ int moe_route_static(int hidden, int n_experts, int topk, const void* x, const v
   const int rc = scratch_for_device(dev, &base);
   if (rc != MOE_OK) return rc;
 
-  // the layer kernel's split (same partial sums), capped by the scratch
-  int ks = gemv_split(hidden, n_experts, n_sms);
-  while (ks > 1 && (size_t)ks * kNoAllocMaxTokens * n_experts * 4 > kPartBytes) {
-    int d = ks - 1;
-    while (d > 1 && (hidden / 256) % d != 0) --d;
-    ks = d;
-  }
+  // the layer kernel's split (same partial sums, so the same routing); a
+  // split whose partial logits do not fit the array is refused rather than
+  // changed (it would change the summation order)
+  const int ks = gemv_split(hidden, n_experts, n_sms);
+  if ((size_t)ks * kNoAllocMaxTokens * n_experts * 4 > kPartBytes)
+    return fail(MOE_ERR_UNSUPPORTED, "this device's router split needs more partial logits than the static scratch holds");
 
   uint8_t* b = static_cast<uint8_t*>(base);
   RouteArgs ra{};
@@ -183,6 +182,22 @@ int moe_route_static(int hidden, int n_experts, int topk, const void* x, const v
   const dim3 grid(((n_experts + 7) / 8) * ks);
   route_kernel_for(hidden / 256)<<<grid, kConsumerWarps * 32, 0, st>>>(ra);
   if ((e = cudaGetLastError()) != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+int moe_route_static_read_status(int* status, moe_stream_t stream) {
+  if (!status) return fail(MOE_ERR_INVALID_ARG, "null status");
+  if (reinterpret_cast<uintptr_t>(status) & 3u) return fail(MOE_ERR_INVALID_ARG, "status must be 4-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
+  void* base = nullptr;
+  const int rc = scratch_for_device(dev, &base);
+  if (rc != MOE_OK) return rc;
+  // the status word is the array's first int (see moe_route_static)
+  if ((e = cudaMemcpyAsync(status, base, sizeof(int), cudaMemcpyDefault,
+                           reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, cudaGetErrorString(e));
   return MOE_OK;
 }
 

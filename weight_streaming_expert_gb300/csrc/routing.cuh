@@ -270,11 +270,12 @@ __device__ __forceinline__ uint32_t ld_relaxed32(const float* p) {
 
 // Words written by other CTAs of the same call while this warp reads them:
 // every word still unwritten is re-read until none is (bounded: after
-// kWaitTimeoutNs the status gets kErrTimeoutGrid and the call's result is
+// `limit` ns the status gets kErrTimeoutGrid and the call's result is
 // undefined).  Planes 0 and 1 are polled together, further planes one each.
 struct PolledPlanes {
   const float* lg;
   size_t plane;
+  unsigned long long limit;
   template <int VPL>
   __device__ __forceinline__ void poll(const float* P, const float* Q, int lane, int E, uint32_t (&w0)[VPL],
                                        uint32_t (&w1)[VPL], int* status) const {
@@ -292,7 +293,7 @@ struct PolledPlanes {
       if (__all_sync(0xffffffffu, ok)) return;
       if (it == 0) {
         t0 = global_timer_ns();
-      } else if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      } else if (global_timer_ns() - t0 > limit) {
         if (lane == 0) set_error(status, kErrTimeoutGrid);
         return;
       }

@@ -102,17 +102,23 @@ class MoELayer:
         torch.cuda.synchronize(self.device)
 
     def forward(self, x, out=None, topk_idx=None, topk_w=None, stream=None, pdl=True, graph=False,
-                trace=False):
-        """x: bf16 [M, H] CUDA.  Returns (out [M,H] bf16, topk_idx [M,k] int32)."""
+                trace=False, out_f32=False, test_skip_arrival=False):
+        """x: bf16 [M, H] CUDA.  Returns (out [M,H], topk_idx [M,k] int32):
+        out is bf16, or with out_f32 the fp32 combine before its rounding (the
+        partial output of one slice of a tensor-parallel split)."""
         M = x.shape[0]
         if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.shape[1] != self.hidden:
             raise ValueError("x must be contiguous bf16 [M, hidden]")
         if out is None:
-            out = torch.empty_like(x)
+            out = torch.empty((M, self.hidden), dtype=torch.float32 if out_f32 else torch.bfloat16,
+                              device=x.device)
+        elif out.dtype != (torch.float32 if out_f32 else torch.bfloat16) or not out.is_contiguous():
+            raise ValueError("out must be contiguous " + ("fp32" if out_f32 else "bf16"))
         if topk_idx is None:
             topk_idx = torch.empty((M, self.topk), dtype=torch.int32, device=x.device)
         flags = ((0 if pdl else N.MOE_FWD_NO_PDL) | (N.MOE_FWD_GRAPH if graph else 0)
-                 | (N.MOE_FWD_TRACE if trace else 0))
+                 | (N.MOE_FWD_TRACE if trace else 0) | (N.MOE_FWD_OUT_F32 if out_f32 else 0)
+                 | (N.MOE_FWD_TEST_SKIP_ARRIVAL if test_skip_arrival else 0))
         rc = N.lib().moe_forward_ex(self._h, _ptr(x), _ptr(out), _ptr(topk_idx), _ptr(topk_w), M,
                                     _stream_ptr(stream), flags)
         N.check("moe_forward_ex", rc)
@@ -130,6 +136,14 @@ class MoELayer:
         rc = N.lib().moe_forward_timed(self._h, _ptr(x), _ptr(out), _ptr(topk_idx), x.shape[0],
                                        _stream_ptr(stream), arr)
         N.check("moe_forward_timed", rc)
+
+    def set_grid(self, ctas: int = 0):
+        """CTAs of every later forward call (0: one per SM).  Synchronises."""
+        N.check("moe_set_grid", N.lib().moe_set_grid(self._h, int(ctas)))
+
+    def set_wait_limit(self, ns: int = 0):
+        """Limit of the kernel's bounded waits in ns (0: the default)."""
+        N.check("moe_set_wait_limit", N.lib().moe_set_wait_limit(self._h, int(ns)))
 
     def read_trace(self):
         """Phase timestamps of the last traced call: int64 numpy [SMs, 16] (ns;
@@ -177,6 +191,36 @@ class MoELayer:
             self.close()
         except Exception:
             pass
+
+
+def tp_slice(w_gate_up, w_down, rank: int, world: int):
+    """The expert weights one GPU of a ``world``-way tensor-parallel split
+    holds (the post's TP4): gate rows and up rows [rank*I/G, (rank+1)*I/G)
+    of every expert and the matching down columns, as contiguous tensors
+    ``(w_gate_up [E, 2I/G, H], w_down [E, H, I/G])`` on the weights' device.
+    The router is not split: every GPU routes all tokens."""
+    E, I2, H = w_gate_up.shape
+    I = I2 // 2
+    if I2 != 2 * I or tuple(w_down.shape) != (E, H, I) or world < 1 or I % world or not 0 <= rank < world:
+        raise ValueError("need w_gate_up [E,2I,H], w_down [E,H,I] and I divisible by world")
+    s = I // world
+    lo, hi = rank * s, (rank + 1) * s
+    gu = torch.cat([w_gate_up[:, lo:hi], w_gate_up[:, I + lo:I + hi]], dim=1).contiguous()
+    return gu, w_down[:, :, lo:hi].contiguous()
+
+
+def combine_partials(parts, out=None, stream=None):
+    """bf16( parts[0] + parts[1] + ... ) in that order, one rounding
+    (``moe_combine_partials``).  parts: fp32 CUDA tensor [G, M, H] (as an
+    all-gather leaves the slices' fp32 outputs).  Returns bf16 [M, H]."""
+    if parts.dtype != torch.float32 or not parts.is_cuda or not parts.is_contiguous() or parts.dim() != 3:
+        raise ValueError("parts must be a contiguous fp32 CUDA tensor [G, M, H]")
+    G, M, H = parts.shape
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=parts.device)
+    N.check("moe_combine_partials", N.lib().moe_combine_partials(_ptr(parts), G, M * H, _ptr(out),
+                                                                 _stream_ptr(stream)))
+    return out
 
 
 class LmHead:

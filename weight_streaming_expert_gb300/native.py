@@ -30,6 +30,8 @@ MOE_GEMV_TENSOR_CORES = 1
 MOE_FWD_NO_PDL = 0x1
 MOE_FWD_GRAPH = 0x2
 MOE_FWD_TRACE = 0x4
+MOE_FWD_OUT_F32 = 0x8
+MOE_FWD_TEST_SKIP_ARRIVAL = 0x40000000
 TRACE_SLOTS = 32
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
@@ -45,7 +47,8 @@ class moe_info_t(ctypes.Structure):
                 ("kernels_per_forward", ctypes.c_int), ("router_split", ctypes.c_int),
                 ("smem_bytes", ctypes.c_size_t), ("shared_expert", ctypes.c_int),
                 ("routed_scale", ctypes.c_float), ("bias_selection_only", ctypes.c_int),
-                ("fp8_experts", ctypes.c_int)]
+                ("fp8_experts", ctypes.c_int), ("grid_ctas", ctypes.c_int),
+                ("wait_limit_ns", ctypes.c_ulonglong)]
 
 
 class moe_layer_opts_t(ctypes.Structure):
@@ -95,6 +98,12 @@ def lib(build_if_missing: bool = True):
         L.moe_set_router_bias.restype = ci
         L.moe_get_status.argtypes = [vp]
         L.moe_get_status.restype = ci
+        L.moe_set_grid.argtypes = [vp, ci]
+        L.moe_set_grid.restype = ci
+        L.moe_set_wait_limit.argtypes = [vp, ctypes.c_ulonglong]
+        L.moe_set_wait_limit.restype = ci
+        L.moe_combine_partials.argtypes = [vp, ci, ctypes.c_size_t, vp, vp]
+        L.moe_combine_partials.restype = ci
         L.moe_get_info.argtypes = [vp, ctypes.POINTER(moe_info_t)]
         L.moe_get_info.restype = ci
         L.moe_read_routing.argtypes = [vp, ci, ip, ip, i32p, i32p, i32p, i32p, f32p, ci]
@@ -103,6 +112,8 @@ def lib(build_if_missing: bool = True):
         L.moe_read_trace.restype = ci
         L.moe_route_static.argtypes = [ci, ci, ci, vp, vp, vp, ci, vp, vp, vp]
         L.moe_route_static.restype = ci
+        L.moe_route_static_read_status.argtypes = [vp, vp]
+        L.moe_route_static_read_status.restype = ci
         L.moe_destroy.argtypes = [vp]
         L.moe_destroy.restype = None
         L.moe_lm_head_create.argtypes = [ci, ci, vp]
