@@ -36,7 +36,8 @@ typedef struct moe_lm_head moe_lm_head_t; /* opaque; owned by the library */
  *   vocab    1..16,777,216 rows (any count: the last tile is zero-padded).
  *   w        device bf16 [vocab][hidden] row-major, 16-byte aligned; read
  *            once here, not kept (the caller may free it afterwards).
- * Synchronises the device.  Returns NULL on error (moe_last_error() says
+ * Synchronises the device before it reads w (work still writing w on any
+ * stream finishes first).  Returns NULL on error (moe_last_error() says
  * why): bad sizes or pointers, a device other than sm_103a, out of memory.
  */
 moe_lm_head_t* moe_lm_head_create(int hidden, int vocab, const void* w);

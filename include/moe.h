@@ -114,8 +114,10 @@ typedef enum {
  *   (re-laid out for streaming: gate/up rows interleaved per expert as in
  *   "Two fusions and a retune", fragment order for the tensor-core loads);
  *   the caller may free its buffers when this returns.  The call is
- *   synchronous on the current device and allocates that device's memory
- *   (weights ~= the input size, plus a few MB of workspace).
+ *   synchronous on the current device: it first waits for all work already
+ *   queued on the device (on any stream: the weights may still be being
+ *   written by it), then allocates that device's memory (weights ~= the
+ *   input size, plus a few MB of workspace) and copies.
  * Returns NULL on error (moe_last_error() says why): invalid sizes or
  *   pointers, a device other than sm_103, or allocation failure.
  */

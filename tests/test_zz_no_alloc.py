@@ -108,7 +108,10 @@ def test_static_routing_matches_the_oracle(oracle, E, k, M, with_bias):
     for m in range(M):
         assert parity.routing_ok(gi[m], ref_idx[m], logits[m]), f"token {m}: {gi[m]} vs {ref_idx[m]}"
         want = ref_w[m] if np.array_equal(gi[m], ref_idx[m]) else oracle.weights_for_set(logits[m], gi[m])
-        np.testing.assert_allclose(gw[m], want, rtol=2e-6, atol=1e-7)
+        # the GPU's logits differ from the oracle's by fp32 summation order
+        # (~3e-6 for a 2560-term dot of this scale); a weight exp(l_j - l_0) / S
+        # moves by a few times that, relatively
+        np.testing.assert_allclose(gw[m], want, rtol=1e-4, atol=1e-6)
         assert abs(float(gw[m].sum()) - 1.0) <= 1e-5
 
 

@@ -279,6 +279,13 @@ moe_lm_head_t* moe_lm_head_create(int hidden, int vocab, const void* w) {
     return nullptr;
   }
   cudaMemset(h->status, 0, sizeof(int));
+  // the caller's weight may still be being written by work queued on any
+  // stream: wait for the device before the re-layout reads it
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+    set_last_error_text(cudaGetErrorString(e));
+    free_lm(h);
+    return nullptr;
+  }
   pack_lm_head_kernel<<<4096, 256>>>(static_cast<const uint4*>(w), reinterpret_cast<uint4*>(h->w), vocab, hidden);
   if ((e = cudaDeviceSynchronize()) != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
     set_last_error_text(cudaGetErrorString(e));

@@ -403,6 +403,14 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   h->ws.y = reinterpret_cast<float*>(base + o_y);
   h->ws.trace = reinterpret_cast<unsigned long long*>(base + o_tr);
 
+  // The caller's weights may still be being written by work it queued on
+  // any stream (a slice, a cast, a copy): the copies below run on a stream
+  // of our own, so wait for everything queued on the device first.
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+    cuda_fail(e, "synchronize before reading the weights");
+    free_layer(h);
+    return nullptr;
+  }
   cudaStream_t s = nullptr;
   if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess) {
     cuda_fail(e, "stream create");
