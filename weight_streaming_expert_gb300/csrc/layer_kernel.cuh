@@ -84,6 +84,7 @@ constexpr uint32_t kOffStatic = 264;  // [1] all consumer warps reduced the stat
 constexpr uint32_t kOffLevel1 = 272;  // [1] every CTA's static gate/up tiles reduced (publisher)
 constexpr uint32_t kOffLevel2 = 280;  // [1] every CTA's gate/up tiles reduced (publisher)
 constexpr uint32_t kOffCall = 288;    // u64: the call's index on the grid counters (1, 2, ...)
+constexpr uint32_t kOffCompacted = 296;  // [1] the compaction is in shared memory (1 arrival)
 constexpr uint32_t kOffTile = 336;    // [8] int: tile id in each gate/up stage (-1: no more)
 constexpr uint32_t kOffDTile = 384;   // [8] int: super-tile id in each down slot (-1: no more)
 constexpr uint32_t kOffDFull = 416;   // [8] down slot: data landed (1 arrival + tx)
@@ -95,7 +96,7 @@ constexpr int kRedSlots = 8;
 constexpr uint32_t kRedBytes = kRedSlots * kConsumerWarps * 32 * 16;
 constexpr int kStaticNum = 7, kStaticDen = 8;  // statically split share of the groups
 static_assert(kMaxGateUpStages <= 8 && kMaxDownStages <= 8, "barrier map");
-static_assert(kOffCall + 8 <= kOffTile && kOffTile + 4 * kMaxGateUpStages <= kOffDTile &&
+static_assert(kOffCall + 8 <= kOffCompacted && kOffCompacted + 8 <= kOffTile && kOffTile + 4 * kMaxGateUpStages <= kOffDTile &&
                   kOffDReady + 8 * kMaxDownStages <= kOffCells &&
                   kOffCells + 4 * kMaxDownStages * kConsumerWarps <= kRingOff,
               "map");
@@ -237,6 +238,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     mbar_init(static_bar, kConsumerWarps);
     mbar_init(level1, 1);
     mbar_init(level2, 1);
+    mbar_init(sb + kOffCompacted, 1);
     for (int d = 0; d < SD; ++d) {
       mbar_init(dfull(d), 1);
       mbar_init(dempty(d), kConsumerWarps);
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     fence_mbar_init();
   }
   for (int e = tid; e < EA; e += kExpertThreads) rt.mask[e] = 0ull;
+  for (int i = tid; i < kChunkLevels * kBitWords; i += kExpertThreads) rt.bits[i] = 0u;
   for (int p = tid; p < NP; p += kExpertThreads) rt.pair_list[p] = 0;
   if (tid < 2) rt.scal[tid] = 0;
 
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       const int p = m * a.K + lane;
       const int idx = rt.s_e[p];
       rt.s_w[p] = VARIANT ? w * a.routed_scale : w;  // the combine's weight; topk_w is unscaled
-      atomicOr(&rt.mask[idx], 1ull << m);
+      bucket_add(rt, idx, m);
       if (blockIdx.x == 0) {
         a.topk_idx[p] = idx;
         if (a.topk_w) a.topk_w[p] = w;
@@ -307,42 +310,19 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int p = MK + tid;
     rt.s_e[p] = a.E;
     rt.s_w[p] = 1.0f;
-    atomicOr(&rt.mask[a.E], 1ull << tid);
+    bucket_add(rt, a.E, tid);
   }
   __syncthreads();
   if (tid == 0) stamp(a, 12);
-  // the reduction area is free until the gate/up loop: scratch for the
-  // pair-axis compaction (small loops: this code runs once per call, with a
-  // cold instruction cache, so its size costs more than its arithmetic)
-  const int n_groups = a.M <= kGroupTokens
-                           ? compact_pairs(rt, NP, a.K, MK, reinterpret_cast<int*>(red), tid, kExpertThreads)
-                           : (compact_masks(rt, NP, a.K, MK, EA), rt.scal[0]);
-  if (tid == 0) stamp(a, 13);
-  if (blockIdx.x == 0) {  // a copy for inspection (moe_read_routing); nothing reads it back
-    for (int i = tid; i < NP; i += kExpertThreads) {
-      a.ws.pair_list[i] = rt.pair_list[i];
-      a.ws.pair_w[i] = rt.s_w[i];
-      if (i < n_groups) {
-        a.ws.grp_expert[i] = rt.grp_expert[i];
-        a.ws.grp_start[i] = rt.grp_start[i];
-        a.ws.grp_cnt[i] = rt.grp_cnt[i];
-      }
-    }
-    if (tid == 0) {
-      *a.ws.n_groups = n_groups;
-      *a.ws.n_active = rt.scal[1];
-    }
-  }
-  if (tid == 0) stamp(a, 3);
-
   const int TPG = 2 * a.I / GU_ROWS;          // gate/up tiles per group
-  const int T_gu = n_groups * TPG;
   const int CL = a.H / (D_ROWS * SPW);        // down cells per group (SPW output slabs each)
   const int SPG = CL / NSL;                   // down super tiles per group
-  const int T_d = n_groups * SPG;
-  // groups [0, g_static) are split statically in both GEMVs: their gate/up
-  // tiles are all in the static share, and so are their down tiles
-  const int g_static = n_groups * kStaticNum / kStaticDen;
+  const int levels = (a.M + kGroupTokens - 1) / kGroupTokens;  // 16-token groups per expert, at most
+  // The producer warp does not wait for the compaction: it numbers the
+  // groups from the chunk bitmaps and starts the gate/up copies at once,
+  // while the other warps compact; the copies' HBM latency hides the
+  // compaction.  The two agree on the group order (ascending expert, then
+  // chunk).
   // The down phase reuses the ring as cells of SPW slabs (d_tile bytes; a
   // gate/up stage is exactly cps cells, the reduction area behind the
   // stages holds the rest).  Gate/up stage (n_gu + r) mod S is released for
@@ -359,36 +339,14 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int p = u * kConsumerWarps + kConsumerWarps - 1;
     return p < gu_cells ? p / cps : S;
   };
-  if (warp == kPublisherWarp) {
-    // =============================================================== publisher
-    if (lane != 0) return;
-    unsigned long long waited = 0;
-    const unsigned long long target = *call_idx * gridDim.x;
-    // static gate/up tiles reduced here -> counted; every CTA counted -> level 1
-    if (!mbar_wait(static_bar, 0, &waited, a.wait_ns)) {
-      record_timeout(a.ws, 2, kErrTimeoutReduce, -3, 0, static_bar, waited);
-      return;
-    }
-    if (!(a.test_flags & kTestSkipArrival) || blockIdx.x != 0) grid_count(a.ws.sync + kSyncStaticDone);
-    stamp(a, 18);
-    if (!grid_wait(a.ws, a.ws.sync + kSyncStaticDone, target, 2, a.wait_ns)) return;
-    mbar_arrive(level1);
-    stamp(a, 6);
-    // all gate/up tiles reduced here -> counted; every CTA counted -> level 2
-    if (!mbar_wait(done, 0, &waited, a.wait_ns)) {
-      record_timeout(a.ws, 2, kErrTimeoutReduce, -4, 0, done, waited);
-      return;
-    }
-    grid_count(a.ws.sync + kSyncGateUpDone);
-    if (!grid_wait(a.ws, a.ws.sync + kSyncGateUpDone, target, 2, a.wait_ns)) return;
-    mbar_arrive(level2);
-    stamp(a, 17);
-    return;
-  }
-
   if (warp == kProducerWarp) {
     // ================================================================ producer
+    const int n_groups = count_groups(rt, EA, levels, lane);
     if (lane != 0) return;
+    stamp(a, 3);
+    const int nw = (EA + 31) / 32;
+    const int T_gu = n_groups * TPG, T_d = n_groups * SPG;
+    const int g_static = n_groups * kStaticNum / kStaticDen;  // as the consumers' (below)
     unsigned long long waited = 0;
     // static share of each phase, then single tiles from the shared tail
     const int Ts = g_static * TPG;
@@ -409,7 +367,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     bool ok = true;
     int level = 0;  // readiness of the h rows seen so far (see the publisher)
     // ---- gate/up tiles
-    int j = 0;
+    int j = 0, gu_w = 0, cur_gg = -1, cur_ge = 0;  // group -> expert lookups (ascending groups)
     for (;; ++j) {
       int tile;
       if (j < n_s) {
@@ -429,9 +387,13 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       stage_tile[s] = tile;
       mbar_arrive(ready(s));
       const int g = tile / TPG, tt = tile - g * TPG;
+      if (g != cur_gg) {  // the compaction's table once it exists, the bitmaps before
+        cur_gg = g;
+        cur_ge = mbar_test_wait(sb + kOffCompacted, 0) ? rt.grp_expert[g] : group_expert(rt, g, levels, nw, gu_w);
+      }
       mbar_arrive_expect_tx(full(s), a.gu_tile);
       bulk_g2s_chunked(ring_u32 + (uint32_t)s * a.gu_tile,
-                       a.w_gate_up + ((size_t)rt.grp_expert[g] * TPG + tt) * a.gu_tile, a.gu_tile, full(s), wpol);
+                       a.w_gate_up + ((size_t)cur_ge * TPG + tt) * a.gu_tile, a.gu_tile, full(s), wpol);
     }
     const int n_gu = j;
     if (ok) {  // end marker for the consumers
@@ -496,6 +458,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     };
     int j2 = 0;
     int cur_dg = -1, cur_de = 0;
+    // the down tiles take their experts from the compaction: wait for it
+    // (it is long done unless this CTA had no gate/up tile at all)
+    if (ok && !mbar_wait(sb + kOffCompacted, 0, &waited, a.wait_ns)) {
+      record_timeout(a.ws, 3, kErrTimeoutReduce, -9, SD, sb + kOffCompacted, waited);
+      ok = false;
+    }
     for (; ok; ++j2) {
       const int s = j2 % SD;
       if (j2 < SD) {
@@ -513,7 +481,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       // the copy first (weights never depend on h), then the id once the
       // group's h rows are ready
       const int g = tile / SPG, q = tile - g * SPG;
-      if (g != cur_dg) {  // the group's expert (smem reads compete with the consumers')
+      if (g != cur_dg) {  // the group's expert (the compaction is in place: see below)
         cur_dg = g;
         cur_de = rt.grp_expert[g];
       }
@@ -566,6 +534,64 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     stamp(a, 10);
     return;
   }
+  // the consumer and publisher warps (288 threads) compact; the reduction
+  // area is free until the gate/up loop: scratch for the pair-axis
+  // compaction (small loops: this code runs once per call, with a cold
+  // instruction cache, so its size costs more than its arithmetic)
+  constexpr int kCompactThreads = kExpertThreads - 32;
+  const int ct = warp < kConsumerWarps ? tid : tid - 32;  // 0 .. 287
+  const int n_groups = a.M <= kGroupTokens
+                           ? compact_pairs(rt, NP, a.K, MK, reinterpret_cast<int*>(red), ct, kCompactThreads)
+                           : (compact_masks(rt, NP, a.K, MK, EA, ct, kCompactThreads), rt.scal[0]);
+  if (tid == 0) {
+    mbar_arrive(sb + kOffCompacted);  // the producer reads grp_expert from here on
+    stamp(a, 13);
+  }
+  if (blockIdx.x == 0) {  // a copy for inspection (moe_read_routing); nothing reads it back
+    for (int i = ct; i < NP; i += kCompactThreads) {
+      a.ws.pair_list[i] = rt.pair_list[i];
+      a.ws.pair_w[i] = rt.s_w[i];
+      if (i < n_groups) {
+        a.ws.grp_expert[i] = rt.grp_expert[i];
+        a.ws.grp_start[i] = rt.grp_start[i];
+        a.ws.grp_cnt[i] = rt.grp_cnt[i];
+      }
+    }
+    if (ct == 0) {
+      *a.ws.n_groups = n_groups;
+      *a.ws.n_active = rt.scal[1];
+    }
+  }
+  // groups [0, g_static) are split statically in both GEMVs: their gate/up
+  // tiles are all in the static share, and so are their down tiles
+  const int g_static = n_groups * kStaticNum / kStaticDen;
+  if (warp == kPublisherWarp) {
+    // =============================================================== publisher
+    if (lane != 0) return;
+    unsigned long long waited = 0;
+    const unsigned long long target = *call_idx * gridDim.x;
+    // static gate/up tiles reduced here -> counted; every CTA counted -> level 1
+    if (!mbar_wait(static_bar, 0, &waited, a.wait_ns)) {
+      record_timeout(a.ws, 2, kErrTimeoutReduce, -3, 0, static_bar, waited);
+      return;
+    }
+    if (!(a.test_flags & kTestSkipArrival) || blockIdx.x != 0) grid_count(a.ws.sync + kSyncStaticDone);
+    stamp(a, 18);
+    if (!grid_wait(a.ws, a.ws.sync + kSyncStaticDone, target, 2, a.wait_ns)) return;
+    mbar_arrive(level1);
+    stamp(a, 6);
+    // all gate/up tiles reduced here -> counted; every CTA counted -> level 2
+    if (!mbar_wait(done, 0, &waited, a.wait_ns)) {
+      record_timeout(a.ws, 2, kErrTimeoutReduce, -4, 0, done, waited);
+      return;
+    }
+    grid_count(a.ws.sync + kSyncGateUpDone);
+    if (!grid_wait(a.ws, a.ws.sync + kSyncGateUpDone, target, 2, a.wait_ns)) return;
+    mbar_arrive(level2);
+    stamp(a, 17);
+    return;
+  }
+
 
   // ================================================================ consumers
   const int g4 = lane >> 2, t4 = lane & 3;

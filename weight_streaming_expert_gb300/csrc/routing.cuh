@@ -408,9 +408,23 @@ __device__ __forceinline__ float topk_dispatch(const Src& src, int ks, const flo
 // Shared-memory routing of one call (ints unless noted):
 //   mask[E] (u64)  s_off[E]  s_e[NP]  s_w[NP] (float)  pair_list[NP]
 //   grp_expert[NP]  grp_start[NP]  grp_cnt[NP]  scal[96]
-// (the compaction comment in the header says how the positions are found)
+//   bits[kChunkLevels][kBitWords] (u32)  pre[kBitWords + 1]
+// (the compaction comment in the header says how the positions are found).
+// bits and pre number the groups without the compaction, for the warp that
+// starts the weight copies while the other warps compact: bit e % 32 of
+// bits[q][e / 32] says expert e's bucket holds more than 16 q pairs (its
+// group q exists) -- the top-k sets it with the atomic OR that adds the
+// (16 q + 1)-th member, since each OR returns the members before it and
+// exactly one sees 16 q of them; pre[w] counts the groups of the experts
+// below 32 w.  Groups run in ascending (expert, q) order, as in the
+// compaction.
+constexpr int kBitWords = (kMaxExperts + 1 + 31) / 32;  // routed experts + a shared one
+constexpr int kChunkLevels = kMaxTokens / kGroupTokens;
+static_assert(kMaxTokens % kGroupTokens == 0 && kMaxTokens <= 64, "u64 token masks in 16-token groups");
+
 __host__ __device__ inline size_t routing_smem_bytes(int NP, int E) {
-  return (size_t)E * 8 + (size_t)E * 4 + (size_t)NP * 4 * 6 + 96 * 4;
+  return (size_t)E * 8 + (size_t)E * 4 + (size_t)NP * 4 * 6 + 96 * 4 + (size_t)kChunkLevels * kBitWords * 4 +
+         (kBitWords + 1) * 4;
 }
 
 struct SmemRouting {
@@ -423,6 +437,8 @@ struct SmemRouting {
   int* grp_start;   // [groups] first sorted position
   int* grp_cnt;     // [groups] pairs in the group (1..16)
   int* scal;        // [0] groups, [1] distinct experts, [8..88) scan scratch
+  unsigned* bits;   // [kChunkLevels][kBitWords] groups that exist, by expert
+  int* pre;         // [kBitWords + 1] groups below each word of experts
 };
 
 __device__ __forceinline__ SmemRouting routing_carve(uint8_t* base, int NP, int E) {
@@ -436,19 +452,113 @@ __device__ __forceinline__ SmemRouting routing_carve(uint8_t* base, int NP, int 
   r.grp_start = r.grp_expert + NP;
   r.grp_cnt = r.grp_start + NP;
   r.scal = r.grp_cnt + NP;
+  r.bits = reinterpret_cast<unsigned*>(r.scal + 96);
+  r.pre = reinterpret_cast<int*>(r.bits + kChunkLevels * kBitWords);
   return r;
+}
+
+// Add pair (token m, expert e) to the buckets (any thread, any order).
+__device__ __forceinline__ void bucket_add(const SmemRouting& r, int e, int m) {
+  const int before = __popcll(atomicOr(&r.mask[e], 1ull << m));
+  if ((before & (kGroupTokens - 1)) == 0)
+    atomicOr(&r.bits[(before / kGroupTokens) * kBitWords + (e >> 5)], 1u << (e & 31));
+}
+
+// One warp, after the buckets are complete: pre[] and the group count
+// (returned to every lane); levels = chunk levels in use, ceil(M / 16).
+// Lane l counts word l (and 32 + l), a five-step scan places them.
+__device__ __forceinline__ int count_groups(const SmemRouting& r, int EA, int levels, int lane) {
+  const int nw = (EA + 31) / 32;
+  int base = 0;
+  for (int w0 = 0; w0 < nw; w0 += 32) {  // one pass unless EA > 1024 (a shared expert beside 1024)
+    const int w = w0 + lane;
+    int c = 0;
+    if (w < nw)
+      for (int q = 0; q < levels; ++q) c += __popc(r.bits[q * kBitWords + w]);
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (w < nw) r.pre[w] = base + inc - c;
+    base += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) r.pre[nw] = base;
+  __syncwarp();
+  return base;
+}
+
+// Position of the n-th (0-based) set bit of a 32-bit word with more than n.
+__device__ __forceinline__ int nth_set_bit32(unsigned w, int n) {
+  int pos = 0;
+#pragma unroll
+  for (int b = 16; b >= 1; b >>= 1) {
+    const int c = __popc(w & ((1u << b) - 1u));
+    if (n >= c) {
+      n -= c;
+      w >>= b;
+      pos += b;
+    }
+  }
+  return pos;
+}
+
+// Expert of group g (< the group count; nw words of experts).  `w` is a
+// cursor: the word of the previous lookup (start at 0).  The word comes from
+// a binary search of pre (lookups with ascending g usually stay in the
+// cursor's word), the expert inside it from a binary search of the groups
+// below each bit position, in registers.
+__device__ __forceinline__ int group_expert(const SmemRouting& r, int g, int levels, int nw, int& w) {
+  if (g < r.pre[w]) w = 0;
+  if (r.pre[w + 1] <= g) {  // largest w' in (w, nw) with pre[w'] <= g
+    int lo = w + 1, hi = nw - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (r.pre[mid] <= g) lo = mid;
+      else hi = mid - 1;
+    }
+    w = lo;
+  }
+  const int j = g - r.pre[w];
+  if (levels == 1) return 32 * w + nth_set_bit32(r.bits[w], j);
+  unsigned B[kChunkLevels];
+#pragma unroll
+  for (int q = 0; q < kChunkLevels; ++q) B[q] = q < levels ? r.bits[q * kBitWords + w] : 0u;
+  auto P = [&](int x) {  // groups of the word's experts below bit x
+    const unsigned m = (1u << x) - 1u;
+    int n = 0;
+#pragma unroll
+    for (int q = 0; q < kChunkLevels; ++q) n += __popc(B[q] & m);
+    return n;
+  };
+  int b = 0;  // the largest bit b with P(b) <= j: its expert holds group g
+#pragma unroll
+  for (int step = 16; step >= 1; step >>= 1)
+    if (b + step <= 31 && P(b + step) <= j) b += step;
+  return 32 * w + b;
+}
+
+// Barrier of the nt threads that run a compaction: the whole CTA, or the
+// consumer and publisher warps (named barrier 3) while the producer warp
+// streams.
+__device__ __forceinline__ void routing_sync(int nt) {
+  if (nt == (int)blockDim.x)
+    __syncthreads();
+  else
+    asm volatile("bar.sync 3, %0;" ::"r"(nt) : "memory");
 }
 
 // Token of pair p: routed pairs p = token * K + slot come first (MK = M * K
 // of them), then the shared expert's pairs MK + token.
 __device__ __forceinline__ int pair_token(int p, int K, int MK) { return p < MK ? p / K : p - MK; }
 
-// Cooperative over the CTA; mask[] and s_e[] complete and visible (a
-// __syncthreads() before).  Bucket sizes and group counts by a block-wide
-// scan over the experts; every pair then takes its place independently.
-// NP pairs (MK routed, see pair_token).  Ends with a __syncthreads().
-__device__ inline void compact_masks(const SmemRouting& r, int NP, int K, int MK, int E) {
-  const int tid = threadIdx.x, nt = blockDim.x;
+// Cooperative over threads tid = 0 .. nt - 1 (the CTA, or the warps that
+// routing_sync counts); mask[] and s_e[] complete and visible (a barrier
+// before).  Bucket sizes and group counts by a scan over the experts; every
+// pair then takes its place independently.  NP pairs (MK routed, see
+// pair_token).  Ends with a barrier.
+__device__ inline void compact_masks(const SmemRouting& r, int NP, int K, int MK, int E, int tid, int nt) {
   // (pairs << 16) + groups share one int (both <= 2048, no carry)
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   int* s_wt = r.scal + 8;
@@ -475,7 +585,7 @@ __device__ inline void compact_masks(const SmemRouting& r, int NP, int K, int MK
     s_wt[warp] = inc;
     s_wa[warp] = ainc;
   }
-  __syncthreads();
+  routing_sync(nt);
   if (warp == 0) {
     int v = lane < nwarps ? s_wt[lane] : 0;
     int va = lane < nwarps ? s_wa[lane] : 0;
@@ -497,7 +607,7 @@ __device__ inline void compact_masks(const SmemRouting& r, int NP, int K, int MK
       r.scal[1] = va;
     }
   }
-  __syncthreads();
+  routing_sync(nt);
   {
     const int base = (warp > 0 ? s_wt[warp - 1] : 0) + inc - packed;
     int c_off = base >> 16, g_off = base & 0xffff;
@@ -514,13 +624,13 @@ __device__ inline void compact_masks(const SmemRouting& r, int NP, int K, int MK
       g_off += (c + kGroupTokens - 1) / kGroupTokens;
     }
   }
-  __syncthreads();
+  routing_sync(nt);
   for (int p = tid; p < NP; p += nt) {
     const int e = r.s_e[p], m = pair_token(p, K, MK);
     const int rank = __popcll(r.mask[e] & ((1ull << m) - 1ull));
     r.pair_list[r.s_off[e] + rank] = p;
   }
-  __syncthreads();
+  routing_sync(nt);
 }
 
 // M <= kGroupTokens: every expert's bucket holds at most M <= 16 pairs, so
@@ -533,15 +643,15 @@ __device__ inline void compact_masks(const SmemRouting& r, int NP, int K, int MK
 // group openers with a smaller expert.  Two short loops over the NP pairs
 // per thread (the code stays small: it runs once per call, cold), no scan.
 // NP pairs (MK routed, see pair_token).  ekey: NP ints of scratch.
-// Cooperative over threads t, t + nt, ...; mask[]
-// and s_e[] complete and visible (a barrier before); scal[0] zero.  Ends
-// with a __syncthreads(); returns the group count.
+// Cooperative over threads t = 0 .. nt - 1 (see routing_sync); mask[] and
+// s_e[] complete and visible (a barrier before); scal[0] zero.  Ends with a
+// barrier; returns the group count.
 __device__ inline int compact_pairs(const SmemRouting& r, int NP, int K, int MK, int* ekey, int t, int nt) {
   for (int p = t; p < NP; p += nt) {
     const int e = r.s_e[p], m = pair_token(p, K, MK);
     ekey[p] = (e << 1) | ((r.mask[e] & ((1ull << m) - 1ull)) == 0ull ? 1 : 0);
   }
-  __syncthreads();
+  routing_sync(nt);
   for (int p = t; p < NP; p += nt) {
     const int ek = ekey[p], e = ek >> 1;
     int below = 0, open_below = 0, same_before = 0;
@@ -560,7 +670,7 @@ __device__ inline int compact_pairs(const SmemRouting& r, int NP, int K, int MK,
       atomicAdd(&r.scal[0], 1);
     }
   }
-  __syncthreads();
+  routing_sync(nt);
   const int n_groups = r.scal[0];
   if (t == 0) r.scal[1] = n_groups;
   return n_groups;
