@@ -350,12 +350,14 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
  * MOE_FWD_TRACE (synchronises the device; profiling aid).
  *   out   host uint64 [cap]: for CTA c, slots [32c, 32c + 32) hold
  *         %globaltimer values in ns: 0 dependency wait passed, 1 router
- *         matvec done, 2 (unused), 3 top-k + compaction done,
+ *         matvec done, 2 (unused), 3 groups counted by the producer warp
+ *         (its first gate/up copies follow at once),
  *         4 first gate/up tile consumed, 5 gate/up loop left, 6 every CTA's
  *         statically split gate/up tiles reduced (publisher), 7 down loop
  *         left, 8 combine done (the CTAs that combine), 9 producer issued
  *         its last gate/up tile, 10 producer issued its last down tile,
- *         12 top-k done, 13 compaction done, 14 first down tile consumed,
+ *         12 top-k done, 13 compaction done (the other warps), 14 first down
+ *         tile consumed,
  *         15 weighted rows of every CTA written (combining CTAs), 17 every
  *         CTA's gate/up tiles reduced (publisher), 18 this CTA's static
  *         gate/up tiles counted in, 19 CTA started, 20 prologue done (before
