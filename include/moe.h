@@ -358,7 +358,9 @@ int moe_read_routing(moe_layer_t* h, int M, int* n_groups, int* n_active,
  *         its last gate/up tile, 10 producer issued its last down tile,
  *         12 top-k done, 13 compaction done (the other warps), 14 first down
  *         tile consumed,
- *         15 weighted rows of every CTA written (combining CTAs), 17 every
+ *         15 combine starts (combining CTAs; calls of more than 8 tokens:
+ *         after every CTA's weighted rows are written, fewer: at once, the
+ *         rows carry their call's index and are polled), 17 every
  *         CTA's gate/up tiles reduced (publisher), 18 this CTA's static
  *         gate/up tiles counted in, 19 CTA started, 20 prologue done (before
  *         the dependency wait).  Slot 11 holds the CTA's gate/up tile COUNT

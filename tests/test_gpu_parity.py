@@ -100,6 +100,7 @@ RAGGED = [
     (3072, 33, 5, 128, 11),
     (2048, 17, 17, 512, 2),
     (2560, 24, 2, 512, 23),
+    (1024, 700, 3, 256, 19),  # more tokens than warps with E > 512: one token per warp at a time
 ]
 
 

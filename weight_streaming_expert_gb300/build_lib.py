@@ -67,11 +67,11 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
         return obj, (r.stdout + r.stderr)
 
-    with ThreadPoolExecutor(max_workers=jobs or min(8, len(srcs))) as ex:
+    with ThreadPoolExecutor(max_workers=jobs or min(len(srcs), max(4, os.cpu_count() or 8))) as ex:
         results = list(ex.map(compile_one, srcs))
-    if verbose:
-        for _, log in results:
-            sys.stdout.write(log)
+    for src, (_, log) in zip(srcs, results):
+        if verbose or "warning" in log:  # compiler warnings are shown, not swallowed
+            sys.stderr.write(f"{os.path.basename(src)}:\n{log}")
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -75,6 +75,9 @@ struct Workspace {
   float* pair_w;             // [kMaxPairs] routing weight by pair id
   __nv_bfloat16* h;          // [kMaxPairs][I] SwiGLU rows, sorted-position order
   float* y;                  // [kMaxPairs][H] weighted down-projection rows, by pair id
+  unsigned long long* yt;    // [kGroupTokens (k + 1)][H] the same for calls of at most kGroupTokens
+                             // tokens: fp32 bits in the low word, the writing call's index (mod 2^32)
+                             // in the high word
   unsigned long long* trace; // [grid][kTraceSlots] phase timestamps (traced calls)
 };
 

@@ -128,6 +128,18 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// A weighted down-projection value with the call index that wrote it: one
+// 64-bit relaxed store, so a reader that sees the index sees the value.
+__device__ __forceinline__ void put_y(unsigned long long* p, float v, unsigned tag) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((unsigned long long)tag << 32) | __float_as_uint(v))
+               : "memory");
+}
+__device__ __forceinline__ unsigned long long get_y(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void stamp(const LayerArgs& a, int slot) {
   if (a.trace) a.ws.trace[(size_t)blockIdx.x * kTraceSlots + slot] = global_timer_ns();
 }
@@ -193,6 +205,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   constexpr bool WA = FP8 && TB == 1;                  // the weights are the MMA's A operand
   constexpr bool TWO = TB == 2;                        // a second token set (group rows 8..15)
   constexpr int NB = FP8 && TB == 2 ? 2 : 1;           // float4 partials per lane (gate/up reduction)
+  constexpr bool kTaggedRows = TB == 1;                // weighted rows tagged with the call index
   const int NSL = kConsumerWarps, SD = a.d_stages;  // cells per down super tile, down slots
   const int SPW = a.d_spw;                           // down slabs per cell
   const int MK = a.M * a.K;                     // routed pairs (token * K + slot)
@@ -774,6 +787,22 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     int pid[2] = {-1, -1};
     float pw[2] = {0.f, 0.f};
     int cur_g = -1, cur_de = 0;
+    // the instances for calls of at most 8 tokens write tagged rows (see the combine)
+    const unsigned ytag = (unsigned)*call_idx;
+    auto put1 = [&](int p, int col, float v) {  // column col of pair p's weighted row
+      if constexpr (kTaggedRows)
+        put_y(a.ws.yt + (size_t)p * a.H + col, v, ytag);
+      else
+        a.ws.y[(size_t)p * a.H + col] = v;
+    };
+    auto put2 = [&](int p, int col, float v0, float v1) {  // columns col, col + 1
+      if constexpr (kTaggedRows) {
+        put_y(a.ws.yt + (size_t)p * a.H + col, v0, ytag);
+        put_y(a.ws.yt + (size_t)p * a.H + col + 1, v1, ytag);
+      } else {
+        *reinterpret_cast<float2*>(a.ws.y + (size_t)p * a.H + col) = make_float2(v0, v1);
+      }
+    };
     for (int j = 0;; ++j) {
       const int s = j % SD;
       const uint32_t ph = (uint32_t)(j / SD) & 1u;
@@ -888,9 +917,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   #pragma unroll
             for (int i = 0; i < 2; ++i)
               if (pid[i] >= 0) {
-                float* yr = a.ws.y + (size_t)pid[i] * a.H + row;
-                yr[0] = pw[i] * (rs.x * (c0[i] + c1[i]));
-                yr[8] = pw[i] * (rs.y * (c0[2 + i] + c1[2 + i]));
+                put1(pid[i], row, pw[i] * (rs.x * (c0[i] + c1[i])));
+                put1(pid[i], row + 8, pw[i] * (rs.y * (c0[2 + i] + c1[2 + i])));
               }
           } else if constexpr (FP8) {
             // block b: (token g4 | g4 + 8) x (rows 16 sl + 8 b + 2 t4, + 1)
@@ -899,22 +927,14 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
             for (int b = 0; b < 2; ++b) {
               const float* v = b ? c1 : c0;
               const float sx = b ? rs.z : rs.x, sy = b ? rs.w : rs.y;
-              if (pid[0] >= 0)
-                *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row + 8 * b) =
-                    make_float2(pw[0] * (sx * v[0]), pw[0] * (sy * v[1]));
-              if (pid[1] >= 0)
-                *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row + 8 * b) =
-                    make_float2(pw[1] * (sx * v[2]), pw[1] * (sy * v[3]));
+              if (pid[0] >= 0) put2(pid[0], row + 8 * b, pw[0] * (sx * v[0]), pw[0] * (sy * v[1]));
+              if (pid[1] >= 0) put2(pid[1], row + 8 * b, pw[1] * (sx * v[2]), pw[1] * (sy * v[3]));
             }
           } else {
             // C: (token g4 | g4 + 8) x (output rows 2 t4, 2 t4 + 1 of the slab)
             const int row = sl * D_ROWS + 2 * t4;
-            if (pid[0] >= 0)
-              *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[0] * a.H + row) =
-                  make_float2(pw[0] * (c0[0] + c1[0]), pw[0] * (c0[1] + c1[1]));
-            if (pid[1] >= 0)
-              *reinterpret_cast<float2*>(a.ws.y + (size_t)pid[1] * a.H + row) =
-                  make_float2(pw[1] * (c0[2] + c1[2]), pw[1] * (c0[3] + c1[3]));
+            if (pid[0] >= 0) put2(pid[0], row, pw[0] * (c0[0] + c1[0]), pw[0] * (c0[1] + c1[1]));
+            if (pid[1] >= 0) put2(pid[1], row, pw[1] * (c0[2] + c1[2]), pw[1] * (c0[3] + c1[3]));
           }
         }
         return true;
@@ -929,47 +949,99 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     if (tid == 0) stamp(a, 7);
   }
 
-  // ---- 6. every CTA's weighted rows written -> combine.  Only the first
-  // n_own_ctas CTAs combine (3 output slabs each: CTA c owns 3c .. 3c+2):
-  // each token's k rows summed in slot order, ONE bf16 rounding.  The other
-  // CTAs count themselves in and leave at once, so the next call's CTAs get
-  // their SMs (and run their prologue) while the combine runs.  (Three slabs
-  // a CTA measured faster than eight: the combine is a latency-bound read
-  // of L2, so more CTAs end it sooner, and at hidden 2560 about 45 SMs are
-  // still left to the next call's prologue.)
+  // ---- 6. combine.  Only the first n_own_ctas CTAs combine (3 output
+  // slabs each: CTA c owns 3c .. 3c+2): each token's k rows summed in slot
+  // order, ONE bf16 rounding.  The other CTAs leave at once, so the next
+  // call's CTAs get their SMs (and run their prologue) while the combine
+  // runs.  (Three slabs a CTA measured faster than eight: the combine is a
+  // latency-bound read of L2, so more CTAs end it sooner, and at hidden 2560
+  // about 45 SMs are still left to the next call's prologue.)  Every CTA
+  // counts itself in once per call: the next call takes its index from that
+  // count.
+  // The instances for calls of at most 8 tokens (TB = 1): every weighted
+  // row value carries the index of the call that wrote it (one 64-bit
+  // store), so an owner polls the values it needs (bounded) and starts as
+  // soon as they are there -- no fence, no count round trip after the last
+  // row.  The others write plain fp32 rows (half the bytes and stores;
+  // measured: at 64 tokens the doubled row traffic cost more than the round
+  // trip saves, and the fp8 consumers of 9..16 tokens, bound by their own
+  // instructions, lost more to the wider stores than the combine gained)
+  // and the owners wait for every CTA's count first.
   const int SLc = a.H / kDownTileRows;  // 8-row output slabs of the combine
   constexpr int kCombineSlabs = 3;
   const int n_own_ctas = min((int)gridDim.x, (SLc + kCombineSlabs - 1) / kCombineSlabs);
   const int own_per = (SLc + n_own_ctas - 1) / n_own_ctas;  // kCombineSlabs unless the grid is small
   const bool owner = (int)blockIdx.x < n_own_ctas;
-  consumers_sync();
-  if (tid == 0) {
-    grid_count(a.ws.sync + kSyncCount);
-    if (owner) grid_wait(a.ws, a.ws.sync + kSyncCount, *call_idx * gridDim.x, 3, a.wait_ns);
+  if constexpr (kTaggedRows) {
+    if (tid == 0) asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(a.ws.sync + kSyncCount) : "memory");
+    if (!owner) return;
+  } else {
+    consumers_sync();  // every weighted row of this CTA written
+    if (tid == 0) {
+      grid_count(a.ws.sync + kSyncCount);
+      if (owner) grid_wait(a.ws, a.ws.sync + kSyncCount, *call_idx * gridDim.x, 3, a.wait_ns);
+    }
+    if (!owner) return;
+    consumers_sync();
   }
-  if (!owner) return;
-  consumers_sync();
   if (tid == 0) stamp(a, 15);
+  const unsigned ctag = (unsigned)*call_idx;
   const int nthr = kConsumerWarps * 32;
   const int sl0 = (int)blockIdx.x * own_per;
   const int n_own = max(0, min(own_per, SLc - sl0));
   const int per = a.M * kDownTileRows;
+  const int KS = a.K + (shared ? 1 : 0);  // the shared slot (pair MK + m) last
+  bool waiting_ok = true;
   for (int it = tid; it < n_own * per; it += nthr) {
     const int sl = sl0 + it / per;
     const int m = (it % per) / kDownTileRows;
     const int r = sl * kDownTileRows + (it % kDownTileRows);
-    const float* yr = a.ws.y + (size_t)m * a.K * a.H + r;
-    const float vs = shared ? __ldcg(a.ws.y + (size_t)(MK + m) * a.H + r) : 0.f;  // the shared slot
     float sum = 0.f;
-    for (int k0 = 0; k0 < a.K; k0 += 8) {  // 8 loads in flight, summed in slot order
-      float v[8];
+    if constexpr (!kTaggedRows) {
+      const float* yr = a.ws.y + (size_t)m * a.K * a.H + r;
+      const float vs = shared ? __ldcg(a.ws.y + (size_t)(MK + m) * a.H + r) : 0.f;  // the shared slot
+      for (int k0 = 0; k0 < a.K; k0 += 8) {  // 8 loads in flight, summed in slot order
+        float v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = k0 + i < a.K ? __ldcg(yr + (size_t)(k0 + i) * a.H) : 0.f;
+        for (int i = 0; i < 8; ++i) v[i] = k0 + i < a.K ? __ldcg(yr + (size_t)(k0 + i) * a.H) : 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (k0 + i < a.K) sum += v[i];
+        for (int i = 0; i < 8; ++i)
+          if (k0 + i < a.K) sum += v[i];
+      }
+      if (shared) sum += vs;  // the shared slot, last
+    } else {
+      auto pair_of = [&](int j) { return j < a.K ? m * a.K + j : MK + m; };
+      for (int k0 = 0; k0 < KS; k0 += 8) {  // 8 values in flight, summed in slot order
+        unsigned long long v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[i] = k0 + i < KS ? get_y(a.ws.yt + (size_t)pair_of(k0 + i) * a.H + r) : ((unsigned long long)ctag << 32);
+        bool all = true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) all = all && (unsigned)(v[i] >> 32) == ctag;
+        if (!all && waiting_ok) {  // not all written yet: poll the missing ones (bounded)
+          const unsigned long long t0 = global_timer_ns();
+          while (!all) {
+            __nanosleep(32);
+            all = true;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if ((unsigned)(v[i] >> 32) != ctag) {
+                v[i] = get_y(a.ws.yt + (size_t)pair_of(k0 + i) * a.H + r);
+                all = all && (unsigned)(v[i] >> 32) == ctag;
+              }
+            if (!all && global_timer_ns() - t0 > a.wait_ns) {
+              record_timeout(a.ws, 3, kErrTimeoutGrid, it, 0, 0, global_timer_ns() - t0);
+              waiting_ok = false;  // the call's result is undefined; finish without waiting
+              break;
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (k0 + i < KS) sum += __uint_as_float((unsigned)v[i]);
+      }
     }
-    if (shared) sum += vs;  // the shared slot, last
     if (a.out_f32)
       a.out_f32[(size_t)m * a.H + r] = sum;  // a partial of a split layer: rounded after the sum of the parts
     else

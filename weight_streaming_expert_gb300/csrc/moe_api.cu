@@ -95,7 +95,7 @@ struct moe_layer {
   uint8_t* w_d = nullptr;   // packed down tiles
   float* bias = nullptr;
   void* ws_mem = nullptr;
-  size_t ws_bytes = 0, weight_bytes = 0;
+  size_t ws_bytes = 0, weight_bytes = 0, yt_bytes = 0;
   Workspace ws{};
   int ks = 1;               // hidden-dim split of the router matvec
   uint32_t tile_gu = 0;     // gate/up tile bytes
@@ -141,6 +141,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 // (the state moe_create leaves).  Only while no kernel of the handle runs.
 void restart_counts(moe_layer* h) {
   cudaMemset(h->ws.sync, 0, kSyncWords * 4);
+  cudaMemset(h->ws.yt, 0, h->yt_bytes);  // call indices restart at 1: no row may carry an old one
   cudaMemset(h->ws.part, 0xff, 2 * (size_t)h->ks * kMaxTokens * h->E * 4);
 }
 
@@ -379,6 +380,8 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   const size_t o_pl = take(np * 4), o_pw = take(np * 4);
   const size_t o_h = take(np * I * 2);
   const size_t o_y = take(np * H * 4);
+  const size_t npt = (size_t)kGroupTokens * h->kp();  // tagged rows: calls of at most kGroupTokens tokens
+  const size_t o_yt = take(npt * H * 8);
   const size_t o_tr = take((size_t)h->n_sms * kTraceSlots * 8);
   h->ws_bytes = off;
   if (ac.alloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
@@ -401,6 +404,8 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   h->ws.pair_w = reinterpret_cast<float*>(base + o_pw);
   h->ws.h = reinterpret_cast<__nv_bfloat16*>(base + o_h);
   h->ws.y = reinterpret_cast<float*>(base + o_y);
+  h->ws.yt = reinterpret_cast<unsigned long long*>(base + o_yt);
+  h->yt_bytes = npt * H * 8;
   h->ws.trace = reinterpret_cast<unsigned long long*>(base + o_tr);
 
   // The caller's weights may still be being written by work it queued on
