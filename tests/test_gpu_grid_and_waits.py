@@ -87,6 +87,40 @@ def test_smaller_grids_match_the_oracle_and_the_full_grid(oracle, ling, ctas):
     layer.set_grid(0)
 
 
+def test_topk_exchange_both_parities_and_a_tiny_grid(ling):
+    """Calls of more tokens than a CTA has warps find each token's top-k once
+    in the grid and exchange the slots through a buffer of the call's parity,
+    which the call clears after use.  Chained calls that take the exchange on
+    both parities, with M changing, equal the same calls made alone; on a
+    4-CTA grid every warp takes several tokens and the results stay the
+    same bits."""
+    layer, _ = ling
+    layer.set_router_bias(None)
+    Ms = [11, 40, 2, 64, 33, 16, 64, 12]
+    xs = [wl.tokens(M, wl.LING.hidden, seed=7_700_000 + i, device=DEV) for i, M in enumerate(Ms)]
+    alone = []
+    for x in xs:
+        out, idx = layer(x)
+        torch.cuda.synchronize()
+        alone.append((out.clone(), idx.clone()))
+    chained = [layer(x) for x in xs]
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    for n, ((o, i), (ro, ri)) in enumerate(zip(chained, alone)):
+        assert torch.equal(i, ri), f"call {n} (M = {Ms[n]}): expert ids differ"
+        assert torch.equal(o.view(torch.int16), ro.view(torch.int16)), f"call {n} (M = {Ms[n]}): outputs differ"
+    layer.set_grid(4)
+    try:
+        small = [layer(xs[n]) for n in (3, 4)]
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        for (o, i), n in zip(small, (3, 4)):
+            assert torch.equal(i, alone[n][1]), f"4 CTAs, M = {Ms[n]}: expert ids differ"
+            assert torch.equal(o.view(torch.int16), alone[n][0].view(torch.int16)), f"4 CTAs, M = {Ms[n]}"
+    finally:
+        layer.set_grid(0)
+
+
 def test_grid_bounds_are_checked(ling):
     from weight_streaming_expert_gb300 import native as N
     layer, _ = ling

@@ -78,6 +78,9 @@ struct Workspace {
   unsigned long long* yt;    // [kGroupTokens (k + 1)][H] the same for calls of at most kGroupTokens
                              // tokens: fp32 bits in the low word, the writing call's index (mod 2^32)
                              // in the high word
+  unsigned long long* xtopk; // [2][kMaxTokens * kMaxTopk] routed slots of calls with more tokens than
+                             // a CTA has warps (odd / even calls): expert id in the high word, weight
+                             // bits in the low word, all ones while unwritten
   unsigned long long* trace; // [grid][kTraceSlots] phase timestamps (traced calls)
 };
 

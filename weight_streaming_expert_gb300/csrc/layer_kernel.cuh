@@ -128,13 +128,16 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 // A weighted down-projection value with the call index that wrote it: one
 // 64-bit relaxed store, so a reader that sees the index sees the value.
 __device__ __forceinline__ void put_y(unsigned long long* p, float v, unsigned tag) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((unsigned long long)tag << 32) | __float_as_uint(v))
                : "memory");
 }
-__device__ __forceinline__ unsigned long long get_y(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
@@ -304,14 +307,60 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
   if (tid == 0) stamp(a, 1);
 
   // ---- 3. top-k of every token, compaction (every CTA, shared memory only)
-  for (int m = warp; m < a.M; m += kExpertThreads / 32) {
-    const float w = topk_dispatch(PolledPlanes{part + (size_t)m * a.E, plane, a.wait_ns}, a.ks, a.bias, a.E, a.K, lane,
-                                  a.ws.status, rt.s_e + m * a.K, VARIANT && a.sel_only != 0);
-    __syncwarp();
-    if (lane < a.K) {
-      const int p = m * a.K + lane;
-      const int idx = rt.s_e[p];
-      rt.s_w[p] = VARIANT ? w * a.routed_scale : w;  // the combine's weight; topk_w is unscaled
+  constexpr int kWarps = kExpertThreads / 32;
+  bool exchanged = false;
+  if constexpr (TB == 2) exchanged = a.M > kWarps;
+  if (!exchanged) {  // every CTA finds every token's top-k itself (a token per warp)
+    for (int m = warp; m < a.M; m += kWarps) {
+      const float w = topk_dispatch(PolledPlanes{part + (size_t)m * a.E, plane, a.wait_ns}, a.ks, a.bias, a.E, a.K,
+                                    lane, a.ws.status, rt.s_e + m * a.K, VARIANT && a.sel_only != 0);
+      __syncwarp();
+      if (lane < a.K) {
+        const int p = m * a.K + lane;
+        const int idx = rt.s_e[p];
+        rt.s_w[p] = VARIANT ? w * a.routed_scale : w;  // the combine's weight; topk_w is unscaled
+        bucket_add(rt, idx, m);
+        if (blockIdx.x == 0) {
+          a.topk_idx[p] = idx;
+          if (a.topk_w) a.topk_w[p] = w;
+        }
+      }
+    }
+  } else if constexpr (TB == 2) {
+    // more tokens than warps: each token's top-k is found ONCE in the grid
+    // (token m by warp m / grid of CTA m mod grid) and published as one
+    // 64-bit word per slot; every CTA then polls the M k words (bounded).
+    // Taking the tokens in turn on one CTA's warps cost ~3 us per token.
+    unsigned long long* xb = a.ws.xtopk + (odd ? (size_t)kMaxTokens * kMaxTopk : 0);
+    int* scratch = reinterpret_cast<int*>(red) + warp * kMaxTopk;  // the warp's slot ids
+    for (int m = (int)blockIdx.x + (int)gridDim.x * warp; m < a.M; m += (int)gridDim.x * kWarps) {
+      const float w = topk_dispatch(PolledPlanes{part + (size_t)m * a.E, plane, a.wait_ns}, a.ks, a.bias, a.E, a.K,
+                                    lane, a.ws.status, scratch, VARIANT && a.sel_only != 0);
+      __syncwarp();
+      if (lane < a.K) {
+        const unsigned long long word =
+            ((unsigned long long)(unsigned)scratch[lane] << 32) | (unsigned long long)__float_as_uint(w);
+        st_relaxed64(xb + m * a.K + lane, word);
+      }
+      __syncwarp();
+    }
+    const unsigned long long t0 = global_timer_ns();
+    for (int i = tid; i < MK; i += kExpertThreads) {
+      unsigned long long word = ld_relaxed64(xb + i);
+      while (word == ~0ull) {  // not published yet (bounded)
+        if (global_timer_ns() - t0 > a.wait_ns) {
+          set_error(a.ws.status, kErrTimeoutGrid);
+          word = 0ull;
+          break;
+        }
+        __nanosleep(32);
+        word = ld_relaxed64(xb + i);
+      }
+      const int m = i / a.K, p = i;
+      const int idx = (int)(word >> 32);
+      const float w = __uint_as_float((unsigned)word);
+      rt.s_e[p] = idx;
+      rt.s_w[p] = VARIANT ? w * a.routed_scale : w;
       bucket_add(rt, idx, m);
       if (blockIdx.x == 0) {
         a.topk_idx[p] = idx;
@@ -593,6 +642,16 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     if (!grid_wait(a.ws, a.ws.sync + kSyncStaticDone, target, 2, a.wait_ns)) return;
     mbar_arrive(level1);
     stamp(a, 6);
+    if constexpr (TB == 2) {
+      // every CTA has read the exchanged slots (its routing precedes its
+      // static tiles): mark this CTA's share of them unwritten for the
+      // next call of this parity
+      if (a.M > kExpertThreads / 32) {
+        unsigned long long* xb = a.ws.xtopk + (odd ? (size_t)kMaxTokens * kMaxTopk : 0);
+        for (int i = (int)blockIdx.x; i < MK; i += (int)gridDim.x)
+          st_relaxed64(xb + i, ~0ull);
+      }
+    }
     // all gate/up tiles reduced here -> counted; every CTA counted -> level 2
     if (!mbar_wait(done, 0, &waited, a.wait_ns)) {
       record_timeout(a.ws, 2, kErrTimeoutReduce, -4, 0, done, waited);
@@ -1015,7 +1074,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         unsigned long long v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          v[i] = k0 + i < KS ? get_y(a.ws.yt + (size_t)pair_of(k0 + i) * a.H + r) : ((unsigned long long)ctag << 32);
+          v[i] = k0 + i < KS ? ld_relaxed64(a.ws.yt + (size_t)pair_of(k0 + i) * a.H + r) : ((unsigned long long)ctag << 32);
         bool all = true;
 #pragma unroll
         for (int i = 0; i < 8; ++i) all = all && (unsigned)(v[i] >> 32) == ctag;
@@ -1027,7 +1086,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if ((unsigned)(v[i] >> 32) != ctag) {
-                v[i] = get_y(a.ws.yt + (size_t)pair_of(k0 + i) * a.H + r);
+                v[i] = ld_relaxed64(a.ws.yt + (size_t)pair_of(k0 + i) * a.H + r);
                 all = all && (unsigned)(v[i] >> 32) == ctag;
               }
             if (!all && global_timer_ns() - t0 > a.wait_ns) {

@@ -139,10 +139,13 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // Arrival counts from zero, every partial logit of both buffers unwritten
 // (the state moe_create leaves).  Only while no kernel of the handle runs.
+constexpr size_t kXtopkBytes = 2 * (size_t)kMaxTokens * kMaxTopk * 8;  // the exchanged top-k slots
+
 void restart_counts(moe_layer* h) {
   cudaMemset(h->ws.sync, 0, kSyncWords * 4);
   cudaMemset(h->ws.yt, 0, h->yt_bytes);  // call indices restart at 1: no row may carry an old one
   cudaMemset(h->ws.part, 0xff, 2 * (size_t)h->ks * kMaxTokens * h->E * 4);
+  cudaMemset(h->ws.xtopk, 0xff, kXtopkBytes);  // every exchanged slot unwritten
 }
 
 // Enqueue the layer kernel.  ev (2 events) brackets it for profiling; the
@@ -382,6 +385,7 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   const size_t o_y = take(np * H * 4);
   const size_t npt = (size_t)kGroupTokens * h->kp();  // tagged rows: calls of at most kGroupTokens tokens
   const size_t o_yt = take(npt * H * 8);
+  const size_t o_xt = take(kXtopkBytes);
   const size_t o_tr = take((size_t)h->n_sms * kTraceSlots * 8);
   h->ws_bytes = off;
   if (ac.alloc(&h->ws_mem, h->ws_bytes) != cudaSuccess) {
@@ -406,6 +410,7 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   h->ws.y = reinterpret_cast<float*>(base + o_y);
   h->ws.yt = reinterpret_cast<unsigned long long*>(base + o_yt);
   h->yt_bytes = npt * H * 8;
+  h->ws.xtopk = reinterpret_cast<unsigned long long*>(base + o_xt);
   h->ws.trace = reinterpret_cast<unsigned long long*>(base + o_tr);
 
   // The caller's weights may still be being written by work it queued on
@@ -425,6 +430,7 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   h->cap_stream = s;
   bool ok = cudaMemsetAsync(h->ws_mem, 0, h->ws_bytes, s) == cudaSuccess &&
             cudaMemsetAsync(h->ws.part, 0xff, part_bytes, s) == cudaSuccess &&  // every logit unwritten
+            cudaMemsetAsync(h->ws.xtopk, 0xff, kXtopkBytes, s) == cudaSuccess &&  // every slot unwritten
             cudaMemcpyAsync(h->w_router, w_router, b_router, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
   if (ok && fp8) {
     pack_gate_up_fp8(static_cast<const uint8_t*>(w_gate_up), h->w_gu, n_experts, inter, hidden, s);
