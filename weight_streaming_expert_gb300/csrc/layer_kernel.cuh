@@ -262,7 +262,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     }
     fence_mbar_init();
   }
-  for (int e = tid; e < EA; e += kExpertThreads) rt.mask[e] = 0ull;
+  for (int e = tid; e < EA; e += kExpertThreads) {
+    rt.mask[e] = 0ull;
+    if constexpr (TB == 2) rt.s_off[e] = 0;  // bucket counts (see bucket_add)
+  }
   for (int i = tid; i < kChunkLevels * kBitWords; i += kExpertThreads) rt.bits[i] = 0u;
   for (int p = tid; p < NP; p += kExpertThreads) rt.pair_list[p] = 0;
   if (tid < 2) rt.scal[tid] = 0;
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
         const int p = m * a.K + lane;
         const int idx = rt.s_e[p];
         rt.s_w[p] = VARIANT ? w * a.routed_scale : w;  // the combine's weight; topk_w is unscaled
-        bucket_add(rt, idx, m);
+        bucket_add<TB == 2>(rt, idx, m);
         if (blockIdx.x == 0) {
           a.topk_idx[p] = idx;
           if (a.topk_w) a.topk_w[p] = w;
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
       const float w = __uint_as_float((unsigned)word);
       rt.s_e[p] = idx;
       rt.s_w[p] = VARIANT ? w * a.routed_scale : w;
-      bucket_add(rt, idx, m);
+      bucket_add<TB == 2>(rt, idx, m);
       if (blockIdx.x == 0) {
         a.topk_idx[p] = idx;
         if (a.topk_w) a.topk_w[p] = w;
@@ -372,7 +375,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) moe_layer_kernel(LayerArgs 
     const int p = MK + tid;
     rt.s_e[p] = a.E;
     rt.s_w[p] = 1.0f;
-    bucket_add(rt, a.E, tid);
+    bucket_add<TB == 2>(rt, a.E, tid);
   }
   __syncthreads();
   if (tid == 0) stamp(a, 12);

@@ -458,8 +458,19 @@ __device__ __forceinline__ SmemRouting routing_carve(uint8_t* base, int NP, int 
 }
 
 // Add pair (token m, expert e) to the buckets (any thread, any order).
+// kNarrow: 32-bit atomics only, a count in s_off[e] (zeroed beforehand;
+// the compaction overwrites it) and the mask's 32-bit half -- two atomics
+// that serialise less on a hot expert than one 64-bit OR (measured: faster
+// from 16 tokens, slower at 6).
+template <bool kNarrow = false>
 __device__ __forceinline__ void bucket_add(const SmemRouting& r, int e, int m) {
-  const int before = __popcll(atomicOr(&r.mask[e], 1ull << m));
+  int before;
+  if constexpr (kNarrow) {
+    before = atomicAdd(&r.s_off[e], 1);
+    atomicOr(reinterpret_cast<unsigned*>(r.mask) + 2 * e + (m >> 5), 1u << (m & 31));
+  } else {
+    before = __popcll(atomicOr(&r.mask[e], 1ull << m));
+  }
   if ((before & (kGroupTokens - 1)) == 0)
     atomicOr(&r.bits[(before / kGroupTokens) * kBitWords + (e >> 5)], 1u << (e & 31));
 }
