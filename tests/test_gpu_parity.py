@@ -113,6 +113,23 @@ def test_ragged_shapes(oracle, MoELayer, H, E, k, I, M):
     layer.close()
 
 
+def test_a_later_smaller_handle_keeps_the_earlier_one_launchable(oracle, MoELayer):
+    """Two handles that run the same kernel instance (same hidden size) with
+    different shared-memory needs (1000 experts need a larger routing area
+    than 16): the instance's dynamic shared-memory limit is a property of the
+    kernel function, so creating the smaller handle second must not make the
+    larger one's launches fail."""
+    big_shape = wl.LayerShape(hidden=256, n_experts=1000, topk=2, inter=128)
+    big, host = small_layer(MoELayer, big_shape, seed=41)
+    small, small_host = small_layer(MoELayer, wl.LayerShape(hidden=256, n_experts=16, topk=2, inter=128), seed=42)
+    assert big.info().smem_bytes > small.info().smem_bytes
+    for M in (3, 12):
+        run_and_check(oracle, big, host, wl.tokens(M, 256, seed=4100 + M).to(DEV), 2)
+        run_and_check(oracle, small, small_host, wl.tokens(M, 256, seed=4200 + M).to(DEV), 2)
+    small.close()
+    big.close()
+
+
 def test_uniform_logits_tie_rule(oracle, MoELayer):
     """W_r = 0: every logit ties, so experts 0..k-1 in order with w = 1/k."""
     shape = wl.LayerShape(hidden=512, n_experts=64, topk=4, inter=128)

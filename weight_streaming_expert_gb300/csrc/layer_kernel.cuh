@@ -31,11 +31,13 @@
 //     follows: a reader polls the words it needs (bounded) until none is
 //     unwritten.
 //  3. EVERY CTA computes the top-k of all tokens and the compaction itself
-//     (shared memory only): nothing else is published and re-read, no
-//     second launch, no last-CTA hand-off.  The results are bitwise equal in all
-//     CTAs (same inputs, same code), so they agree on every position.  With
-//     at most 16 tokens every chosen expert is one group and the compaction
-//     is worked out on the pair axis (two short loops, no scan).
+//     (shared memory only): no second launch, no last-CTA hand-off.  The
+//     results are bitwise equal in all CTAs (same inputs, same code), so they
+//     agree on every position.  With more tokens than a CTA has warps, each
+//     token's top-k is found once in the grid and its k slots published as
+//     64-bit words that every CTA polls (one token a warp, not several in
+//     turn).  With at most 16 tokens every chosen expert is one group and the
+//     compaction is worked out on the pair axis (two short loops, no scan).
 //  4. Gate/up: (group, 8-row) tiles of 8 weight rows x H, staged by the
 //     producer with bulk copies into a ring of mbarrier-guarded stages.
 //     The tiles of the first 7/8 of the groups are split statically, the
@@ -60,9 +62,11 @@
 //     hands the tile id to the consumers (its copy is already in flight).
 //     The static down share holds (nearly) only early groups, so in practice
 //     nothing waits.
-//  6. Combine: once every CTA's weighted rows are written (a grid-wide
-//     count), CTA c sums the k rows of each token for the 8-row output slabs
-//     c, c + grid, ... in slot order, with ONE bf16 rounding.
+//  6. Combine: the first CTAs (3 output slabs each) sum the k weighted rows
+//     of each token in slot order, with ONE bf16 rounding.  Calls of up to 8
+//     tokens write each weighted value with the index of the call that wrote
+//     it in one 64-bit word, and the combining CTAs poll the values; larger
+//     calls wait for a grid-wide count of all CTAs first.
 // Every wait is bounded: a timeout sets a sticky status bit, records where,
 // and the thread carries on (the call's result is then undefined).
 #pragma once

@@ -458,11 +458,14 @@ moe_layer* create_layer(int hidden, int n_experts, int topk, int inter, const vo
   }
   // The expert kernels run one CTA per SM with most of its shared memory;
   // asking for the largest carveout up front avoids a reconfiguration of the
-  // L1/shared split between launches.
+  // L1/shared split between launches.  The dynamic shared-memory limit is a
+  // property of the kernel function, shared by every handle that launches
+  // it: it is set to the device's opt-in maximum, so that a handle created
+  // later with a smaller need never lowers it below an earlier handle's.
   e = cudaSuccess;
   for (int i = 0; i < 2 && e == cudaSuccess; ++i)
     if ((e = cudaFuncSetAttribute(h->plan[i].kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)h->plan[i].smem_max)) == cudaSuccess)
+                                  (int)prop.sharedMemPerBlockOptin)) == cudaSuccess)
       e = cudaFuncSetAttribute(h->plan[i].kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) {
     cuda_fail(e, "shared-memory attribute");
